@@ -1,0 +1,456 @@
+"""Benchmark of the paged FP8 MLA decode step on GB300.
+
+One step = the whole hot path over one batch: ``mla_kv_append`` of the step's
+new tokens (Q per request) into their page slots, then ``mla_decode`` (split
+kernel + log-sum-exp combine) over every request's pages. Inputs are seeded
+synthetic workloads (``paged_mla_decode_gb300.workloads``) resident in HBM.
+
+Default workload: single-user long context -- batch 1, 64 heads, one query
+token, 100,000 cached tokens, FP8 e4m3 cache, page size 64. The cache (57.6 MB)
+would fit in L2, so R independent copies of it (different shuffled pages,
+R * size >= 4 x L2) are rotated step by step.
+
+Output: one JSON line (rank 0). ``value`` is the algorithmic KV bandwidth in
+GB/s (unique cache bytes read per step / step time); steps/s, tokens/s and the
+fraction of the measured HBM peak ride along. ``--impl reference`` times the
+float64 CPU oracle on the same workload instead.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_mla_decode_gb300 import accounting  # noqa: E402
+from paged_mla_decode_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "paged FP8 MLA decode: KV HBM GB/s (% of GB300 peak) and decode steps/sec"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES_FALLBACK = 129 * 1024 * 1024
+
+CONFIGS = {
+    "long": (lambda: wl.long_context(), "e4m3",
+             "single-user long context: B=1 H=64 Q=1 L=100000, FP8 e4m3 cache, page 64"),
+    "tiny": (lambda: wl.tiny(), "e4m3", "tiny: B=2 H=16 Q=1 L={1024,777}, e4m3, page 64"),
+    "concurrent": (lambda: wl.concurrent(), "e4m3",
+                   "concurrent decode: B=32 H=64 Q=1 L~U[60k,140k], FP8 e4m3 cache"),
+    "concurrent_bf16": (lambda: wl.concurrent(), "bf16",
+                        "concurrent decode: B=32 H=64 Q=1 L~U[60k,140k], BF16 cache"),
+    "prefix_shared": (lambda: wl.prefix_shared(), "e4m3",
+                      "prefix-shared: 16 groups x 4 forks, 120k shared prefix, e4m3"),
+    "speculative": (lambda: wl.speculative(), "e4m3",
+                    "speculative decode: B=32 Q=4 causal drafts, L~logN(142k), e4m3"),
+}
+
+
+def _rank_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def aggregate(values_ms, units_per_rank):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    t = max(values_ms)
+    return sum(units_per_rank) / (t / 1e3), t
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.t0 = None
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "50"]
+            if gpu_id:
+                cmd += ["-i", gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags)
+                          if f.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def _profile_traffic(kernel_sources):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "decode_long_ncu.json")
+    try:
+        with open(path) as f:
+            prof = json.load(f)
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for src in kernel_sources:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if prof.get("source_sha256") != h.hexdigest():
+        return None
+    return prof.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline field)
+# ---------------------------------------------------------------------------
+def _oracle_sample_step(w, pages_ref, b, start_page, n_tokens):
+    from oracle import attention as oatt
+    table = w.block_table[b:b + 1, start_page:].copy()
+    lens = np.array([n_tokens], np.int32)
+    return oatt.decode(w.q_bits[b:b + 1, :1], pages_ref, table, lens, w.sm_scale, w.kv_scale)
+
+
+def _oracle_pages(w, kv_dtype, max_tokens):
+    """Oracle-encoded pages of request 0 (or as many tokens as max_tokens)."""
+    from oracle import e4m3 as oe4m3
+    pages = np.zeros((w.num_pages, 64, 576), dtype=np.uint8 if kv_dtype == "e4m3" else np.uint16)
+    flat = pages.reshape(-1, 576)
+    seg = w.request_segments[0][0]
+    bits = w.segment_latent(seg)[:max_tokens]
+    slots = w.segment_slots(seg)[:max_tokens]
+    flat[slots] = oe4m3.encode(oe4m3.bf16_bits_to_f64(bits), w.kv_scale) if kv_dtype == "e4m3" \
+        else bits
+    return pages
+
+
+def cpu_oracle_rate(w, kv_dtype, seconds=15.0, n_tokens=None, steps=None):
+    """Oracle throughput on request 0 of the workload: GB/s of KV and seconds per token."""
+    L0 = int(w.seq_lens[0])
+    n = min(L0, n_tokens or L0)
+    pages = _oracle_pages(w, kv_dtype, n)
+    bpt = accounting.kv_bytes_per_token(kv_dtype)
+    times = []
+    t_start = time.perf_counter()
+    k = 0
+    while True:
+        t0 = time.perf_counter()
+        _oracle_sample_step(w, pages, 0, 0, n)
+        times.append(time.perf_counter() - t0)
+        k += 1
+        if steps is not None and k >= steps:
+            break
+        if steps is None and time.perf_counter() - t_start >= seconds:
+            break
+    per = sum(times) / len(times)
+    return n * bpt / per / 1e9, per / n, n, len(times)
+
+
+def run_reference(args):
+    rank, world, _ = _rank_env()
+    if rank != 0:
+        return 0
+    make, kv_dtype, desc = CONFIGS[args.config]
+    w = make()
+    L0 = int(w.seq_lens[0])
+    # calibrate: the whole run (warmup + steps) should take about two minutes
+    _, sec_per_tok, _, _ = cpu_oracle_rate(w, kv_dtype, n_tokens=min(L0, 4096), steps=1)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(64, min(L0, budget / sec_per_tok)))
+    from oracle import attention as oatt  # noqa: F401
+    pages = _oracle_pages(w, kv_dtype, n)
+    for _ in range(args.warmup):
+        _oracle_sample_step(w, pages, 0, 0, n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_sample_step(w, pages, 0, 0, n)
+    dt = time.perf_counter() - t0
+    per_step = dt / args.steps
+    bpt = accounting.kv_bytes_per_token(kv_dtype)
+    value = n * bpt / per_step / 1e9
+    sample = (f"{n} of the {L0} tokens of request 0, all {w.num_heads} heads, per step "
+              f"(float64 numpy oracle, BLAS threads = default)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "kv_dtype": kv_dtype},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+
+    from paged_mla_decode_gb300 import binding
+
+    rank, world, local = _rank_env()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load_library()
+
+    make, kv_dtype, desc = CONFIGS[args.config]
+    w = make()
+    B, Q, H = w.batch, w.num_queries, w.num_heads
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", L2_BYTES_FALLBACK)
+    bpt = accounting.kv_bytes_per_token(kv_dtype)
+    unique_bytes = w.unique_tokens * bpt
+    copies = args.copies or max(1, math.ceil(4 * l2 / unique_bytes))
+    maps, tables = w.cache_copies(copies)
+
+    # ---- resident inputs: R cache copies filled through mla_kv_append ----
+    dt = torch.uint8 if kv_dtype == "e4m3" else torch.bfloat16
+    kv_scale = w.kv_scale if kv_dtype == "e4m3" else 1.0
+    pages = torch.zeros((copies * w.num_pages, 64, 576), dtype=dt, device=dev)
+    chunk = 1 << 16
+    for si in range(len(w.segments)):
+        bits = w.segment_latent(si)
+        for a in range(0, bits.shape[0], chunk):
+            x = torch.from_numpy(bits[a:a + chunk].view(np.int16)).view(torch.bfloat16).to(dev)
+            lat, rope = x[:, :512].contiguous(), x[:, 512:].contiguous()
+            for r in range(copies):
+                slots = torch.from_numpy(w.segment_slots(si, maps[r])[a:a + chunk]).to(dev)
+                binding.mla_kv_append(lat, rope, slots, pages, kv_scale)
+    torch.cuda.synchronize()
+    del x, lat, rope
+
+    q = torch.from_numpy(w.q_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    seq_lens = torch.from_numpy(w.seq_lens).to(dev)
+    tables_d = [torch.from_numpy(t).to(dev) for t in tables]
+    fresh = torch.from_numpy(w.fresh_token_latent().view(np.int16)).view(torch.bfloat16).to(dev)
+    fresh_lat, fresh_rope = fresh[:, :512].contiguous(), fresh[:, 512:].contiguous()
+    base_slots = w.fresh_token_slots().astype(np.int64)
+    fresh_slots = []
+    for r in range(copies):
+        page, off = base_slots // 64, base_slots % 64
+        fresh_slots.append(torch.from_numpy((maps[r][page] * 64 + off).astype(np.int32)).to(dev))
+    out = torch.empty((B, Q, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
+    ws = torch.zeros(binding.mla_decode_workspace_size(B, Q, H), dtype=torch.uint8, device=dev)
+
+    def step(r, ev=None):
+        binding.mla_kv_append(fresh_lat, fresh_rope, fresh_slots[r], pages, kv_scale)
+        if ev is not None:
+            ev[0].record()
+        binding.mla_decode(q, pages, tables_d[r], seq_lens, w.sm_scale, kv_scale, out, lse, ws)
+        if ev is not None:
+            ev[1].record()
+
+    # ---- one CUDA graph per cache copy; decode bracketed by external events ----
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for r in range(copies):
+            step(r)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True, external=True),
+            torch.cuda.Event(enable_timing=True, external=True)) for _ in range(copies)]
+    graphs = []
+    for r in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(r, evs[r])
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % copies].replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record()
+        for i in range(args.steps):
+            graphs[i % copies].replay()
+        t_end.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    decode_ms = [a.elapsed_time(b) for a, b in evs]
+    decode_us = 1e3 * sum(decode_ms) / len(decode_ms)
+
+    if dist:
+        tt = torch.tensor([elapsed_ms], dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    status = binding.read_device_status(ws)
+    steps_per_s = args.steps / (elapsed_ms / 1e3)
+    sb = accounting.step_bytes(w.seq_lens, Q, H, kv_dtype, unique_tokens=w.unique_tokens)
+    kv_gbs = world * sb["kv"] * steps_per_s / 1e9
+    tokens_per_s = world * B * Q * steps_per_s
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+        h_q, h_lens = pin(q), pin(seq_lens)
+        h_tables = [pin(t) for t in tables_d]
+        h_lat, h_rope = pin(fresh_lat), pin(fresh_rope)
+        h_slots = [pin(s) for s in fresh_slots]
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        d_q, d_lens, d_table = torch.empty_like(q), torch.empty_like(seq_lens), torch.empty_like(
+            tables_d[0])
+        d_lat, d_rope, d_slots = (torch.empty_like(fresh_lat), torch.empty_like(fresh_rope),
+                                  torch.empty_like(fresh_slots[0]))
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_lens, h_tables[0], h_lat, h_rope,
+                                                           h_slots[0]))
+        d2h = out.numel() * out.element_size() + lse.numel() * lse.element_size()
+        n_e2e = max(1, min(args.steps, args.e2e_steps))
+
+        def e2e_step(r):
+            with torch.cuda.stream(stream):
+                for d, h in ((d_q, h_q), (d_lens, h_lens), (d_table, h_tables[r]),
+                             (d_lat, h_lat), (d_rope, h_rope), (d_slots, h_slots[r])):
+                    d.copy_(h, non_blocking=True)
+                binding.mla_kv_append(d_lat, d_rope, d_slots, pages, kv_scale)
+                binding.mla_decode(d_q, pages, d_table, d_lens, w.sm_scale, kv_scale, out, lse, ws)
+                h_out.copy_(out, non_blocking=True)
+                h_lse.copy_(lse, non_blocking=True)
+            stream.synchronize()
+
+        for i in range(min(args.warmup, 20)):
+            e2e_step(i % copies)
+        t0 = time.perf_counter()
+        for i in range(n_e2e):
+            e2e_step(i % copies)
+        e2e_dt = (time.perf_counter() - t0) / n_e2e
+        e2e = {"value": world * sb["kv"] / e2e_dt / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "ms_per_step": e2e_dt * 1e3}
+
+    peak, peak_kind = measured_peaks()
+    decode_bytes = sb["total"]
+    achieved = decode_bytes / (decode_us * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": _profile_traffic(
+                    ["paged_mla_decode_gb300/csrc/decode_mma.cu"]),
+                "kernel": "mla_decode call (split decode kernel + LSE combine kernel)",
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
+                "measured" else "fallback 6.8 TB/s",
+                "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_us": decode_us}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, _, n_tok, n_steps = cpu_oracle_rate(w, kv_dtype, seconds=args.cpu_seconds)
+        cpu = {"value": rate, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{n_steps} full oracle decode(s) of request 0 ({n_tok} tokens, "
+                         f"{H} heads), float64 numpy, BLAS threads = default"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": kv_gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16" if kv_dtype == "e4m3" else
+            "bf16", "data": "synthetic",
+            "config": {"workload": desc, "batch": B, "queries": Q, "heads": H,
+                       "seq_lens_total": int(w.seq_lens.sum()), "unique_tokens": w.unique_tokens,
+                       "kv_dtype": kv_dtype, "page_size": 64,
+                       "l2": f"rotating {copies} cache copies "
+                             f"({copies * unique_bytes / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
+                       "parallelism": f"replicas x{world}"},
+            "steps_per_s": world * steps_per_s, "tokens_per_s": tokens_per_s,
+            "kv_gbs": kv_gbs, "pct_of_hbm_peak": 100.0 * kv_gbs / peak,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 3 * args.steps, "clocks": clocks,
+            "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(CONFIGS), default="long")
+    ap.add_argument("--copies", type=int, default=0, help="cache copies rotated (0 = auto)")
+    ap.add_argument("--e2e-steps", type=int, default=300)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

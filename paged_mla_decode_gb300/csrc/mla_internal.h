@@ -1,0 +1,30 @@
+// mla_internal.h -- host-side declarations shared by the library's .cu files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+// Typed views of a decode workspace (see WorkspaceLayout in mla_common.cuh).
+struct DecodeWorkspace {
+  unsigned* status;
+  int32_t* row_base;
+  int32_t* row_np;
+  int32_t* piece_err;
+  float* part_lse;
+  float* part_out;
+};
+
+// Merge the pieces written by a decode kernel into out (bf16) and lse (fp32).
+cudaError_t launch_combine_pieces(const DecodeWorkspace& ws, int rows, int heads,
+                                  int max_pieces_per_row, __nv_bfloat16* out, float* lse,
+                                  cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace mla
