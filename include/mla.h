@@ -182,6 +182,43 @@ MLA_API mla_status mla_decode(const void* q, const void* kv_pages, int64_t num_p
 MLA_API mla_status mla_decode_combine(const float* part_out, const float* part_lse, int num_parts,
                               int64_t num_rows, void* out, float* lse, mla_stream_t stream);
 
+/*
+ * mla_decode_static_scratch -- mla_decode for callers that cannot allocate.
+ *
+ * No counterpart on the pages: this entry point exists for callers that may not
+ * allocate device memory when they decode -- plug-ins inside an engine that has
+ * reserved all device memory in its own pool and gives them no allocator, or
+ * serving loops that forbid cudaMalloc (which can synchronise the device) after
+ * start-up. It computes exactly what mla_decode computes, with the same kernels
+ * and arguments, but takes no workspace: the split-KV scratch lives in one
+ * array of MLA_STATIC_SCRATCH_BYTES inside this library's device image, held by
+ * every GPU that loads the library until the process exits. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ *  - Limit: returns MLA_ERR_WORKSPACE, enqueuing nothing, when the problem needs
+ *    more scratch than MLA_STATIC_SCRATCH_BYTES, i.e. when
+ *    mla_decode_workspace_size(batch, num_queries, num_heads, num_ctas) exceeds
+ *    it: at 64 heads with one CTA per SM on a 152-SM GPU, batch x num_queries
+ *    may be at most 358 rows.
+ *  - Set-up: the first call on each device looks up the array's device address
+ *    with that device current (cudaGetSymbolAddress). Make that first call
+ *    before any stream capture.
+ *  - Sharing: every call on a device uses the same array, which keeps the last
+ *    call's contents. Calls that overlap on the GPU (for instance on two
+ *    streams) race and give wrong results: order them on one stream or with
+ *    events.
+ *  - device_status: optional device pointer (may be NULL) that receives this
+ *    call's MLA_DEVICE_ERR_* bits; the copy in the array is cleared afterwards.
+ */
+#define MLA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+MLA_API mla_status mla_decode_static_scratch(const void* q, const void* kv_pages, int64_t num_pages,
+                                             int page_size, int kv_dtype,
+                                             const int32_t* block_table, int max_pages,
+                                             const int32_t* seq_lens, int batch, int num_queries,
+                                             int num_heads, float sm_scale, float kv_scale,
+                                             int num_ctas, void* out, float* lse,
+                                             unsigned* device_status, mla_stream_t stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

@@ -28,7 +28,8 @@ MLA_DEVICE_ERR_BAD_PAGE = 0x1
 MLA_DEVICE_ERR_BAD_LENGTH = 0x2
 
 EXPORTED = ("mla_abi_version", "mla_status_string", "mla_kv_append",
-            "mla_decode_workspace_size", "mla_decode", "mla_decode_combine")
+            "mla_decode_workspace_size", "mla_decode", "mla_decode_combine",
+            "mla_decode_static_scratch")
 
 _lib = None
 
@@ -66,6 +67,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_decode_combine.restype = c.c_int
     lib.mla_decode_combine.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_void_p,
                                        c.c_void_p, c.c_void_p]
+    lib.mla_decode_static_scratch.restype = c.c_int
+    lib.mla_decode_static_scratch.argtypes = [
+        c.c_void_p, c.c_void_p, c.c_int64, c.c_int, c.c_int, c.c_void_p, c.c_int, c.c_void_p,
+        c.c_int, c.c_int, c.c_int, c.c_float, c.c_float, c.c_int, c.c_void_p, c.c_void_p,
+        c.c_void_p, c.c_void_p]
     _lib = lib
     return lib
 
@@ -152,6 +158,37 @@ def mla_decode_combine(part_out: torch.Tensor, part_lse: torch.Tensor, out: torc
     st = load_library().mla_decode_combine(_ptr(part_out), _ptr(part_lse), num_parts, rows,
                                            _ptr(out), _ptr(lse), _stream(stream))
     _check(st, "mla_decode_combine")
+
+
+def mla_decode_static_scratch(q: torch.Tensor, kv_pages: torch.Tensor,
+                              block_table: torch.Tensor, seq_lens: torch.Tensor, sm_scale: float,
+                              kv_scale: float, out: torch.Tensor, lse: torch.Tensor,
+                              device_status: torch.Tensor | None = None, num_ctas: int = 0,
+                              stream=None) -> None:
+    """mla_decode without a workspace, for callers that cannot allocate device memory.
+
+    The split-KV scratch is a fixed array inside libmla.so (MLA_STATIC_SCRATCH_BYTES),
+    shared by every call on a device: calls must not overlap on the GPU. The first
+    call on a device looks up the array's address and should precede any stream
+    capture. ``device_status`` (int32, one element, optional) receives the call's
+    MLA_DEVICE_ERR_* bits.
+    """
+    assert q.dtype == torch.bfloat16 and q.dim() == 4 and q.shape[3] == 576 and q.is_contiguous()
+    batch, nq, heads, _ = q.shape
+    assert block_table.dtype == torch.int32 and block_table.dim() == 2
+    assert block_table.is_contiguous() and block_table.shape[0] == batch
+    assert seq_lens.dtype == torch.int32 and seq_lens.numel() == batch
+    assert out.dtype == torch.bfloat16 and tuple(out.shape) == (batch, nq, heads, 512)
+    assert lse.dtype == torch.float32 and tuple(lse.shape) == (batch, nq, heads)
+    assert kv_pages.is_contiguous() and kv_pages.dim() == 3 and kv_pages.shape[2] == 576
+    if device_status is not None:
+        assert device_status.dtype == torch.int32 and device_status.numel() >= 1
+    st = load_library().mla_decode_static_scratch(
+        _ptr(q), _ptr(kv_pages), int(kv_pages.shape[0]), int(kv_pages.shape[1]),
+        kv_dtype_code(kv_pages), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+        batch, nq, heads, float(sm_scale), float(kv_scale), int(num_ctas), _ptr(out), _ptr(lse),
+        _ptr(device_status), _stream(stream))
+    _check(st, "mla_decode_static_scratch")
 
 
 def read_device_status(workspace: torch.Tensor) -> int:
