@@ -128,19 +128,21 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def _profile_traffic(kernel_sources):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+def _profile_traffic():
+    """DRAM bytes per launch from the committed ncu record, if its kernel source is unchanged.
+
+    ``profiles/decode_long_ncu.json`` names the source file it was taken from and
+    that file's sha256; a mismatch (the kernel changed since) gives None.
+    """
     path = os.path.join(ROOT, "profiles", "decode_long_ncu.json")
     try:
         with open(path) as f:
             prof = json.load(f)
-    except Exception:
+        with open(os.path.join(ROOT, prof["source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, KeyError, ValueError):
         return None
-    h = hashlib.sha256()
-    for src in kernel_sources:
-        with open(os.path.join(ROOT, src), "rb") as f:
-            h.update(f.read())
-    if prof.get("source_sha256") != h.hexdigest():
+    if prof.get("source_sha256") != digest:
         return None
     return prof.get("dram_bytes_per_launch")
 
@@ -393,8 +395,7 @@ def run_gpu(args):
     decode_bytes = sb["total"]
     achieved = decode_bytes / (decode_us * 1e-6) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": _profile_traffic(
-                    ["paged_mla_decode_gb300/csrc/decode_mma.cu"]),
+                "frac": achieved / peak, "traffic": _profile_traffic(),
                 "kernel": "mla_decode call (split decode kernel + LSE combine kernel)",
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                 "measured" else "fallback 6.8 TB/s",

@@ -83,6 +83,7 @@ typedef enum mla_kv_dtype {
 /* Bits of the device status word (first 4 bytes of the decode workspace). */
 #define MLA_DEVICE_ERR_BAD_PAGE 0x1u   /* a block-table entry outside the cache */
 #define MLA_DEVICE_ERR_BAD_LENGTH 0x2u /* seq_len < num_queries or > max_pages*page_size */
+#define MLA_DEVICE_ERR_TIMEOUT 0x4u    /* an internal pipeline wait ran out (2 s); results invalid */
 
 /* Version of this ABI (increments on any incompatible change). */
 MLA_API int mla_abi_version(void);

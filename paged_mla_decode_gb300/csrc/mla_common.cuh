@@ -106,6 +106,7 @@ struct RowCursor {
   int64_t rt;     // first global tile of row r
   int t;          // tiles of row r
   int base;       // first partial slot of row r
+  int n;          // visible tokens of row r
 };
 
 __device__ inline void cursor_next_row(const Plan& p, RowCursor& cur) {
@@ -113,7 +114,8 @@ __device__ inline void cursor_next_row(const Plan& p, RowCursor& cur) {
     cur.base += p.row_pieces(cur.rt, cur.t);
     cur.rt += cur.t;
     cur.r += 1;
-    cur.t = cur.r < p.rows() ? p.row_tiles(cur.r) : 0;
+    cur.n = cur.r < p.rows() ? p.row_tokens(cur.r) : 0;
+    cur.t = cur.n <= 0 ? 0 : (cur.n + p.tile - 1) / p.tile;
   } while (cur.t == 0 && cur.r < p.rows());
 }
 
@@ -136,7 +138,7 @@ __device__ inline RowCursor plan_find_row_warp(const Plan& p, int64_t x0, bool w
   int lane = threadIdx.x & 31;
   int64_t rt_carry = 0;
   int base_carry = 0;
-  RowCursor found{-1, 0, 0, 0};
+  RowCursor found{-1, 0, 0, 0, 0};
   bool have = false;
   for (int r0 = 0; r0 < p.rows(); r0 += 32) {
     int r = r0 + lane;
@@ -171,6 +173,7 @@ __device__ inline RowCursor plan_find_row_warp(const Plan& p, int64_t x0, bool w
       found.rt = __shfl_sync(0xffffffffu, rt, src);
       found.t = __shfl_sync(0xffffffffu, t, src);
       found.base = __shfl_sync(0xffffffffu, base, src);
+      found.n = __shfl_sync(0xffffffffu, r < p.rows() ? p.row_tokens(r) : 0, src);
       have = true;
       if (!write_table) break;
     }

@@ -19,6 +19,25 @@ struct DecodeWorkspace {
   float* part_out;
 };
 
+// Everything a decode kernel launch needs (validated by the caller).
+struct DecodeLaunch {
+  const __nv_bfloat16* q;
+  const uint8_t* kv;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  int batch, nq, heads;
+  bool bf16;         // cache holds bf16 (else e4m3 codes)
+  float score_mul;   // sm_scale * log2(e) * kv_scale
+  float kv_scale;
+  int G;             // CTAs launched
+  DecodeWorkspace ws;
+};
+
+// Split-KV decode on the tcgen05 tensor cores (decode_tc.cu); heads <= 64.
+cudaError_t launch_decode_tensor_core(const DecodeLaunch& d, cudaStream_t stream);
+
 // Merge the pieces written by a decode kernel into out (bf16) and lse (fp32).
 cudaError_t launch_combine_pieces(const DecodeWorkspace& ws, int rows, int heads,
                                   int max_pieces_per_row, __nv_bfloat16* out, float* lse,
