@@ -73,30 +73,34 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ out_base, in
   if (tid == 0) *lse_out = empty ? -INFINITY : m + logf(total);
 }
 
-// Merge of mla_decode's pieces. One block per (row, head, half of the 512 dims):
-// the 8 warps take every 8th piece, each lane 8 consecutive dims, so the loads of
-// many pieces are in flight at once; warps then add their sums in shared memory.
+// Merge of mla_decode's pieces. One block per (row, head, quarter of the 512 dims):
+// the 8 warps take every 8th piece and each lane 4 consecutive dims, with 4
+// pieces per warp in flight; the warps then add their sums in shared memory.
+// Launched as a programmatic dependent of the decode kernel: its prologue runs
+// while the decode kernel drains, and griddepcontrol.wait orders the reads.
 constexpr int kPieceThreads = 256;
 constexpr int kPieceWarps = kPieceThreads / 32;
+constexpr int kQuarters = 4;
 
 __global__ void __launch_bounds__(kPieceThreads)
 combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __restrict__ row_np,
                       const int32_t* __restrict__ piece_err, const float* __restrict__ part_lse,
                       const float* __restrict__ part_out, int heads,
                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  __shared__ float s_acc[kPieceWarps][256];
+  __shared__ float4 s_acc[kPieceWarps][32];
   __shared__ float s_red[kPieceWarps];
   __shared__ int s_bad;
   const int64_t blk = blockIdx.x;
-  const int half = (int)(blk & 1);
-  const int64_t rh = blk >> 1;
+  const int quarter = (int)(blk % kQuarters);
+  const int64_t rh = blk / kQuarters;
   const int r = (int)(rh / heads);
   const int h = (int)(rh - (int64_t)r * heads);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) s_bad = 0;
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // decode kernel's writes are visible
+  __syncthreads();
   const int np = row_np[r];
   const int base = row_base[r];
-  if (tid == 0) s_bad = 0;
-  __syncthreads();
   for (int s = tid; s < np; s += kPieceThreads)
     if (piece_err[base + s]) s_bad = 1;
   // max of the pieces' lse
@@ -112,56 +116,58 @@ combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __res
   for (int w = 1; w < kPieceWarps; ++w) m = fmaxf(m, s_red[w]);
   const bool empty = np <= 0 || s_bad || !(m > -INFINITY);
   __syncthreads();
-  // weighted sums: warp w takes pieces w, w+8, ...; lane takes dims [8*lane, 8*lane+8)
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  // weighted sums: warp w takes pieces w, w+8, ...; lane takes dims [4*lane, 4*lane+4)
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (!empty) {
-    // four pieces per warp in flight at a time
+    const int64_t dim0 = 128 * quarter + 4 * lane;
     for (int s0 = warp; s0 < np; s0 += 4 * kPieceWarps) {
       float wgt[4];
-      float4 a[4], b[4];
+      float4 v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int s = s0 + u * kPieceWarps;
         wgt[u] = 0.f;
-        a[u] = b[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (s < np) {
           const int64_t piece = (int64_t)(base + s) * heads + h;
           const float l = part_lse[piece];
           wgt[u] = (l > -INFINITY) ? fast_exp2((l - m) * kLog2e) : 0.f;
-          const float4* src =
-              reinterpret_cast<const float4*>(part_out + piece * kDLatent + 256 * half + 8 * lane);
-          a[u] = src[0];
-          b[u] = src[1];
+          v[u] = *reinterpret_cast<const float4*>(part_out + piece * kDLatent + dim0);
         }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (wgt[u] == 0.f) continue;  // empty piece: its output is never read
         wsum += wgt[u];
-        acc[0] += wgt[u] * a[u].x; acc[1] += wgt[u] * a[u].y;
-        acc[2] += wgt[u] * a[u].z; acc[3] += wgt[u] * a[u].w;
-        acc[4] += wgt[u] * b[u].x; acc[5] += wgt[u] * b[u].y;
-        acc[6] += wgt[u] * b[u].z; acc[7] += wgt[u] * b[u].w;
+        acc.x += wgt[u] * v[u].x;
+        acc.y += wgt[u] * v[u].y;
+        acc.z += wgt[u] * v[u].z;
+        acc.w += wgt[u] * v[u].w;
       }
     }
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) s_acc[warp][8 * lane + i] = acc[i];
+  s_acc[warp][lane] = acc;
   if (lane == 0) s_red[warp] = wsum;
   __syncthreads();
-  float total = 0.f;
+  if (warp == 0) {
+    float total = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int w = 0; w < kPieceWarps; ++w) total += s_red[w];
-  // thread t finalises dim t of this half
-  float v = 0.f;
-#pragma unroll
-  for (int w = 0; w < kPieceWarps; ++w) v += s_acc[w][tid];
-  v = empty ? 0.f : v / total;
-  out[rh * kDLatent + 256 * half + tid] = __float2bfloat16_rn(v);
-  if (half == 0 && tid == 0) lse[rh] = empty ? -INFINITY : m + logf(total);
+    for (int w = 0; w < kPieceWarps; ++w) {
+      total += s_red[w];
+      const float4 b = s_acc[w][lane];
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    const float inv = empty ? 0.f : 1.0f / total;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * inv, a.w * inv);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out + rh * kDLatent + 128 * quarter + 4 * lane) = packed;
+    if (quarter == 0 && lane == 0) lse[rh] = empty ? -INFINITY : m + logf(total);
+  }
 }
 
 // Standalone merge: part_out [S][rows][512], part_lse [S][rows]; one block per row.
@@ -181,10 +187,18 @@ cudaError_t launch_combine_pieces(const DecodeWorkspace& ws, int rows, int heads
                                   int max_pieces_per_row, __nv_bfloat16* out, float* lse,
                                   cudaStream_t stream) {
   (void)max_pieces_per_row;
-  const int64_t blocks = (int64_t)rows * heads * 2;
-  combine_pieces_kernel<<<(unsigned)blocks, kPieceThreads, 0, stream>>>(
-      ws.row_base, ws.row_np, ws.piece_err, ws.part_lse, ws.part_out, heads, out, lse);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((int64_t)rows * heads * kQuarters));
+  cfg.blockDim = dim3(kPieceThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_pieces_kernel, ws.row_base, ws.row_np, ws.piece_err,
+                            (const float*)ws.part_lse, (const float*)ws.part_out, heads, out, lse);
 }
 
 }  // namespace mla

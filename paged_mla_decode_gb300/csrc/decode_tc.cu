@@ -3,14 +3,14 @@
 // One CTA per SM walks its run of cache pages (split-KV planner in
 // mla_common.cuh) in tiles of up to 128 tokens (two pages of one request row).
 // Warp roles:
-//   warps 0-3  softmax + epilogue: thread t owns TMEM lane t (token t of the
-//              tile's scores; dim t of each 128-dim block of the output)
-//   warps 4-7  load + convert: 16-byte loads of the page bytes into registers,
-//              several 8 KB chunks ahead, e4m3 -> f16 ("the FP8 attention kernel
-//              has to convert values as it reads them": "Smaller, faster, safer:
-//              running Kimi and GLM at scale", section "Quantizing the KV cache"),
-//              stored into a 128-byte-swizzled shared tile; q staging per piece
-//   warp 8     TMEM allocation and the single thread that issues tcgen05.mma
+//   warps 0-3   softmax + epilogue: thread t owns TMEM lane t (token t of the
+//               tile's scores; dim t of each 128-dim block of the output);
+//               warp 0 allocates TMEM and its thread 0 issues every tcgen05.mma
+//   warps 4-11  load + convert: 16-byte loads of the page bytes into registers,
+//               up to three 4 KB jobs ahead per warp, e4m3 -> f16 (an FP8 cache
+//               is widened as it is read: "Smaller, faster, safer: running Kimi
+//               and GLM at scale", section "Quantizing the KV cache"), stored
+//               into a 128-byte-swizzled shared tile; q by TMA once per piece
 // Per tile, two dense contractions share one shared-memory tile of the 128
 // tokens x 576 entry dims (all heads attend over one latent head: "vLLM x
 // AgentX", section "Kimi K3"):
@@ -65,20 +65,22 @@ constexpr int kOffAlpha = kOffLSum + 256;
 constexpr int kOffRed = kOffAlpha + 256;                   // float [4][64] per-warp maxima
 constexpr int kOffRedSum = kOffRed + 1024;                 // float [2][4][64] per-warp sums
 constexpr int kOffFlags = kOffRedSum + 2048;               // int [4]
-constexpr int kOffBar = kOffFlags + 16;                    // uint64 [28]
-constexpr int kNumBars = 24;
+constexpr int kOffBar = kOffFlags + 16;                    // uint64 [kNumBars]
+constexpr int kNumBars = 20;
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;               // slack for 1024 alignment
 
 // barrier indices
 constexpr int BAR_CHUNK_FULL = 0;     // [9]  load warps -> MMA (count 2: both halves)
-constexpr int BAR_CHUNK_EMPTY = 9;    // [9]  MMA commit -> load warps
-constexpr int BAR_Q_EMPTY = 18;       // MMA commit -> load warps (q tile free)
-constexpr int BAR_S_FULL = 19;        // [2] MMA commit -> softmax
-constexpr int BAR_O_FULL = 21;        // MMA commit -> epilogue
-constexpr int BAR_DRAIN = 22;         // MMA commit before TMEM is freed
-constexpr int BAR_Q_TMA = 23;         // TMA bytes of q landed (count 1 + tx bytes)
+constexpr int BAR_CHUNK_EMPTY = 9;    // [5]  MMA commit -> load warps: chunks 2i and 2i+1
+                                      //      (the 128-dim block PV block i reads), chunk 8
+constexpr int BAR_Q_EMPTY = 14;       // MMA commit -> load warps (q tile free)
+constexpr int BAR_S_FULL = 15;        // [2] MMA commit -> softmax
+constexpr int BAR_O_FULL = 17;        // MMA commit -> epilogue
+constexpr int BAR_DRAIN = 18;         // MMA commit before TMEM is freed
+constexpr int BAR_Q_TMA = 19;         // TMA bytes of q landed (count 1 + tx bytes)
+__device__ __forceinline__ int empty_bar(int chunk) { return BAR_CHUNK_EMPTY + (chunk >> 1); }
 
 
 enum Flag { F_ABORT = 0, F_PIECE_BAD = 1 };
@@ -209,6 +211,8 @@ __global__ void __maxnreg__(168)
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (uint32_t)i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the combine kernel may be scheduled now; it waits for this grid's writes itself
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   // ---- planning (shared by all roles) ----
   __shared__ int64_t s_plan[6];
@@ -219,7 +223,8 @@ __global__ void __maxnreg__(168)
   }
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      tc::mbar_init(bar(i), i < BAR_CHUNK_EMPTY ? 2 : 1);  // chunk: two half-chunk jobs
+      // chunk full: every load warp (e4m3 slices) or both half-chunk jobs (bf16)
+      tc::mbar_init(bar(i), i < BAR_CHUNK_EMPTY ? (kBf16 ? 2 : kLoadWarps) : 1);
     }
     tc::fence_mbar_init();
     flags[F_ABORT] = 0;
@@ -261,18 +266,142 @@ __global__ void __maxnreg__(168)
   if (x_begin < x_end) {
     if (warp >= kSoftmaxWarps) {
       // =================== load + convert warps ===================
-      // A tile is 18 jobs: chunk c (64 dims) x half h (64 tokens = one page). Job g of
+      const int lw = warp - kSoftmaxWarps;  // 0..7
+      const int lt = tid - 32 * kSoftmaxWarps;
+      bool aborted = false;
+      // q[b][j][0:H][:] arrives by TMA, one 64-dim chunk per copy, already in the
+      // 128-byte-swizzled layout (the softmax warps convert it to f16).
+      auto issue_q = [&](int r) {
+        tc::mbar_arrive_expect_tx(bar(BAR_Q_TMA), (uint32_t)(kChunks * H * 128));
+        for (int ch = 0; ch < kChunks; ++ch)
+          tc::tma_load_2d(sbase + kOffQ + ch * kQChunkBytes, &q_map, 64 * ch, r * H,
+                          bar(BAR_Q_TMA));
+      };
+      // rows H..63 of the Q tile stay zero (padded heads); TMA writes only rows < H
+      if (H < kN) {
+        for (int v = lt; v < kChunks * (kN - H) * 8; v += kLoadThreads) {
+          const int ch = v / ((kN - H) * 8), rem = v - ch * (kN - H) * 8;
+          const int row = H + (rem >> 3), unit = rem & 7;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(
+                           sbase + kOffQ + ch * kQChunkBytes + row * 128 + (unit << 4)),
+                       "r"(0u));
+        }
+        tc::fence_proxy_async_smem();
+      }
+
+      if constexpr (!kBf16) {
+        // e4m3 cache: load warp lw owns tokens [16 lw, 16 lw + 16) of every tile (its
+        // page is the tile's page lw / 4). Per tile a lane holds 18 16-byte vectors:
+        // vector g*9 + c covers token 8g + lane/4 of the slice, dims 64c + 16 (lane%4)
+        // .. +15, so each warp load reads 8 whole 64-byte row pieces. A chunk is
+        // converted as soon as the previous tile's PV has released it, and its
+        // registers are refilled at once with the next tile's bytes: the loads of
+        // tile k+1 are in flight while tile k is multiplied.
+        const uint64_t pol = l2_evict_first_policy();
+        const int slice0 = 16 * (lw & 3);   // first token of the slice within its page
+        const int page_sel = lw >> 2;       // which page of the tile
+        struct Slice {
+          const uint8_t* base;  // this lane's first byte (token 8*0 + lane/4, dims 16 (lane%4))
+          uint32_t vis;         // bit g: token 8g + lane/4 of the slice is visible
+          int r;                // request row of the tile (for q)
+          bool ps;              // first tile of a piece
+        };
+        auto slice_of = [&](const TileWalker& w) {
+          Slice sl;
+          const int valid = w.valid_tokens() - 64 * page_sel - slice0;  // tokens of my slice
+          int page = -1;
+          if (page_sel < w.npages)
+            page = __ldg(p.block_table + (int64_t)(w.cur.r / p.nq) * p.max_pages +
+                         w.page_in_row() + page_sel);
+          const bool page_ok = page >= 0 && (int64_t)page < p.num_pages;
+          const int tok = lane >> 2;
+          sl.vis = (page_ok && tok < valid ? 1u : 0u) | (page_ok && tok + 8 < valid ? 2u : 0u);
+          sl.base = p.kv + (page_ok ? (int64_t)page : 0) * (kPageSize * kDEntry) +
+                    (int64_t)(slice0 + tok) * kDEntry + 16 * (lane & 3);
+          sl.r = w.cur.r;
+          sl.ps = w.piece_start();
+          return sl;
+        };
+        // masked vectors read the pool's first bytes (and are zeroed at conversion)
+        auto load_slice_chunk = [&](uint4 (&b)[18], const Slice& sl, int c) {
+          b[c] = ld_stream_16((sl.vis & 1u) ? sl.base + 64 * c : p.kv, pol);
+          b[9 + c] = ld_stream_16((sl.vis & 2u) ? sl.base + 8 * kDEntry + 64 * c : p.kv, pol);
+        };
+        uint4 buf[18];
+        TileWalker nw;
+        nw.init(plan, cur0, x_begin, x_end);
+        Slice cur = slice_of(nw);
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) load_slice_chunk(buf, cur, c);
+        int piece_seen = 0;
+        for (int64_t k = 0;; ++k) {
+          nw.next();
+          const bool have_next = !nw.done();
+          Slice nxt = cur;
+          if (have_next) nxt = slice_of(nw);
+          if (cur.ps) {
+            // load warp 0 fetches q for a piece once the previous piece's QK is done
+            if (lw == 0 && lane == 0) {
+              if (piece_seen > 0 &&
+                  !tc::mbar_wait(bar(BAR_Q_EMPTY), (uint32_t)((piece_seen - 1) & 1), kWaitNs))
+                aborted = true;
+              else
+                issue_q(cur.r);
+            }
+            ++piece_seen;
+          }
+          if (__any_sync(0xffffffffu, aborted)) {
+            aborted = true;
+            break;
+          }
+          const uint32_t par = (uint32_t)((k - 1) & 1);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) {
+            if (k > 0 && (c & 1) == 0 && !tc::mbar_wait(bar(empty_bar(c)), par, kWaitNs)) {
+              aborted = true;
+              break;
+            }
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+              uint4 v = buf[9 * g + c];
+              if (!((cur.vis >> g) & 1u)) v = make_uint4(0, 0, 0, 0);
+              const int token = 64 * page_sel + slice0 + 8 * g + (lane >> 2);
+              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+              uint32_t h[8];
+#pragma unroll
+              for (int i2 = 0; i2 < 4; ++i2) {
+                h[2 * i2] = e4m3x2_to_f16x2((uint16_t)(w4[i2] & 0xffffu));
+                h[2 * i2 + 1] = e4m3x2_to_f16x2((uint16_t)(w4[i2] >> 16));
+              }
+              const uint32_t a0 = sbase + kv_tile_off(token, 2 * (lane & 3), c);
+              const uint32_t a1 = sbase + kv_tile_off(token, 2 * (lane & 3) + 1, c);
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a0), "r"(h[0]),
+                           "r"(h[1]), "r"(h[2]), "r"(h[3]));
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a1), "r"(h[4]),
+                           "r"(h[5]), "r"(h[6]), "r"(h[7]));
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(BAR_CHUNK_FULL + c));
+            if (have_next) load_slice_chunk(buf, nxt, c);
+          }
+          if (aborted || !have_next) break;
+          cur = nxt;
+        }
+      } else {
+      // =================== load + convert warps ===================
+      // bf16 cache: a tile is 18 jobs: chunk c (64 dims) x half h (64 tokens = one page). Job g of
       // the CTA's sequence goes to load warp g % 8, so the warps convert different
       // chunks at the same time; each warp keeps its next kDepth jobs in flight in
       // registers. A chunk is full when the warps of both halves have arrived.
-      const int lw = warp - kSoftmaxWarps;  // 0..7
-      const int lt = tid - 32 * kSoftmaxWarps;
       constexpr int kVec = kBf16 ? 16 : 8;   // 16-byte vectors per lane per job
-      constexpr int kDepth = kBf16 ? 1 : 2;  // jobs in flight per warp
+      // jobs in flight per warp: a tile's 18 jobs over 8 warps leave 3 to some
+      // warps, so 3 keeps the whole next tile in registers while PV runs
+      constexpr int kDepth = kBf16 ? 2 : 3;
       constexpr int kJobsPerTile = 2 * kChunks;
-      uint4 buf[kDepth + 1][kVec];
-      uint32_t bufmask[kDepth + 1];
-      bool aborted = false;
+      const uint64_t pol = l2_evict_first_policy();
+      uint4 buf[kDepth][kVec];
+      uint32_t bufmask[kDepth];
 
       // job walker: tile cursor + page ids of the current tile
       struct JobCursor {
@@ -321,30 +450,10 @@ __global__ void __maxnreg__(168)
           const bool ok = page_ok && token < valid;
           const uint8_t* src = pbase + token * (kDEntry * (kBf16 ? 2 : 1)) +
                                chunk * (kBf16 ? 128 : 64) + part * 16;
-          dst[k] = __ldg(reinterpret_cast<const uint4*>(ok ? src : p.kv));
+          dst[k] = ld_stream_16(ok ? src : p.kv, pol);
           mask |= (ok ? 1u : 0u) << k;
         }
       };
-      // q[b][j][0:H][:] arrives by TMA, one 64-dim chunk per copy, already in the
-      // 128-byte-swizzled layout (the softmax warps convert it to f16).
-      auto issue_q = [&](const TileWalker& tw) {
-        tc::mbar_arrive_expect_tx(bar(BAR_Q_TMA), (uint32_t)(kChunks * H * 128));
-        for (int ch = 0; ch < kChunks; ++ch)
-          tc::tma_load_2d(sbase + kOffQ + ch * kQChunkBytes, &q_map, 64 * ch, tw.cur.r * H,
-                          bar(BAR_Q_TMA));
-      };
-      // rows H..63 of the Q tile stay zero (padded heads); TMA writes only rows < H
-      if (H < kN) {
-        for (int v = lt; v < kChunks * (kN - H) * 8; v += kLoadThreads) {
-          const int ch = v / ((kN - H) * 8), rem = v - ch * (kN - H) * 8;
-          const int row = H + (rem >> 3), unit = rem & 7;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(
-                           sbase + kOffQ + ch * kQChunkBytes + row * 128 + (unit << 4)),
-                       "r"(0u));
-        }
-        tc::fence_proxy_async_smem();
-      }
-
       JobCursor issue, comp;
       jc_init(issue);
       jc_init(comp);
@@ -359,13 +468,8 @@ __global__ void __maxnreg__(168)
       }
       while (!comp.tw.done() && !aborted) {
 #pragma unroll
-        for (int s = 0; s < kDepth + 1; ++s) {
+        for (int s = 0; s < kDepth; ++s) {
           if (comp.tw.done() || aborted) break;
-          if (!issue.tw.done()) {  // refill the slot the previous job has left
-            load_job(buf[(s + kDepth) % (kDepth + 1)], bufmask[(s + kDepth) % (kDepth + 1)],
-                     issue);
-            jc_next(issue);
-          }
           const int jj = (int)(comp.g - comp.tile * kJobsPerTile);
           const int chunk = jj >> 1, half = jj & 1;
           if (comp.tile != last_tile) {
@@ -376,7 +480,7 @@ __global__ void __maxnreg__(168)
                     !tc::mbar_wait(bar(BAR_Q_EMPTY), (uint32_t)((piece_seen - 1) & 1), kWaitNs))
                   aborted = true;
                 else
-                  issue_q(comp.tw);
+                  issue_q(comp.tw.cur.r);
               }
               ++piece_seen;
             }
@@ -386,7 +490,7 @@ __global__ void __maxnreg__(168)
             aborted = true;
             break;
           }
-          if (comp.tile > 0 && !tc::mbar_wait(bar(BAR_CHUNK_EMPTY + chunk),
+          if (comp.tile > 0 && !tc::mbar_wait(bar(empty_bar(chunk)),
                                               (uint32_t)((comp.tile - 1) & 1), kWaitNs)) {
             aborted = true;
             break;
@@ -422,8 +526,13 @@ __global__ void __maxnreg__(168)
           tc::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(bar(BAR_CHUNK_FULL + chunk));
+          if (!issue.tw.done()) {  // refill the slot just converted
+            load_job(buf[s], bufmask[s], issue);
+            jc_next(issue);
+          }
           jc_next(comp);
         }
+      }
       }
       if (aborted) {
         flags[F_ABORT] = 1;
@@ -506,20 +615,25 @@ __global__ void __maxnreg__(168)
           named_bar_softmax();  // q tile and qmul ready
         }
         // ---- thread 0: S^T = K Q^T for this tile, as its chunks arrive ----
+        // (fully unrolled with descriptors formed as base + constant: a tcgen05.mma
+        // whose descriptors are computed at run time issues at half the rate)
         bool mma_ok = true;
         if (t == 0) {
-          const uint32_t id_qk = tc::idesc_f16(128, kN, kBf16, false, false);
-          const uint32_t k_a = sbase + kOffK, q_a = sbase + kOffQ;
-          tc::fence_after_sync();
-          for (int ch = 0; ch < kChunks; ++ch) {
-            mma_ok = tc::mbar_wait(bar(BAR_CHUNK_FULL + ch), (uint32_t)(k & 1), kWaitNs);
-            if (!mma_ok) break;
-            tc::fence_after_sync();
+          constexpr uint32_t id_qk = tc::idesc_f16(128, kN, kBf16, false, false);
+          const uint64_t a0 = tc::smem_desc_sw128(sbase + kOffK, 16, 1024);
+          const uint64_t b0 = tc::smem_desc_sw128(sbase + kOffQ, 16, 1024);
+          const uint32_t d_s = tmem + s_col(sb);
+          const uint32_t par = (uint32_t)(k & 1);
 #pragma unroll
-            for (int sub = 0; sub < 4; ++sub) {
-              const uint64_t a = tc::smem_desc_sw128(k_a + ch * kChunkBytes + sub * 32, 16, 1024);
-              const uint64_t b = tc::smem_desc_sw128(q_a + ch * kQChunkBytes + sub * 32, 16, 1024);
-              tc::mma_f16_ss(tmem + s_col(sb), a, b, id_qk, (ch | sub) != 0);
+          for (int ch = 0; ch < kChunks; ++ch) {
+            if (mma_ok) mma_ok = tc::mbar_wait(bar(BAR_CHUNK_FULL + ch), par, kWaitNs);
+            if (mma_ok) {
+              tc::fence_after_sync();
+#pragma unroll
+              for (int sub = 0; sub < 4; ++sub)
+                tc::mma_f16_ss(d_s, a0 + (uint64_t)((ch * kChunkBytes + sub * 32) >> 4),
+                               b0 + (uint64_t)((ch * kQChunkBytes + sub * 32) >> 4), id_qk,
+                               (ch | sub) != 0);
             }
           }
           if (mma_ok) {
@@ -669,21 +783,20 @@ __global__ void __maxnreg__(168)
         named_bar_softmax();  // every row of P written, rescale done, red[] free
         if (t == 0) {
           // ---- thread 0: O^T += V^T P^T (V = the tile's first 512 dims, MN-major view) ----
-          const uint32_t id_pv = tc::idesc_f16(128, kN, kBf16, true, true);
-          const uint32_t k_a = sbase + kOffK, p_a = k_a + 8 * kChunkBytes;
+          constexpr uint32_t id_pv = tc::idesc_f16(128, kN, kBf16, true, true);
+          const uint64_t a0 = tc::smem_desc_sw128(sbase + kOffK, kChunkBytes, 1024);
+          const uint64_t b0 = tc::smem_desc_sw128(sbase + kOffK + 8 * kChunkBytes, 16, 1024);
+          const uint32_t d_o = tmem + kOCol;
           tc::fence_after_sync();
+#pragma unroll
           for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t a =
-                  tc::smem_desc_sw128(k_a + (2 * mt) * kChunkBytes + kk * 2048, kChunkBytes, 1024);
-              const uint64_t b = tc::smem_desc_sw128(p_a + kk * 2048, 16, 1024);
-              tc::mma_f16_ss(tmem + kOCol + 64 * mt, a, b, id_pv, !(ps && kk == 0));
-            }
-            tc::mma_commit(bar(BAR_CHUNK_EMPTY + 2 * mt));
-            tc::mma_commit(bar(BAR_CHUNK_EMPTY + 2 * mt + 1));
+            for (int kk = 0; kk < 8; ++kk)
+              tc::mma_f16_ss(d_o + 64 * mt, a0 + (uint64_t)((2 * mt * kChunkBytes + kk * 2048) >> 4),
+                             b0 + (uint64_t)((kk * 2048) >> 4), id_pv, !(ps && kk == 0));
+            tc::mma_commit(bar(BAR_CHUNK_EMPTY + mt));
           }
-          tc::mma_commit(bar(BAR_CHUNK_EMPTY + 8));
+          tc::mma_commit(bar(empty_bar(8)));
           if (pe) tc::mma_commit(bar(BAR_O_FULL));
         }
         {

@@ -202,6 +202,21 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // e4m3 pair -> f16 pair (exact: every e4m3 value is an f16 normal number).
+// L2 policy for data read once (the KV stream): its lines are the first to be
+// evicted, so that code, q and page tables stay resident in L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+// 16-byte read-only load that allocates no L1 line and marks its L2 lines with `pol`.
+__device__ __forceinline__ uint4 ld_stream_16(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(v));

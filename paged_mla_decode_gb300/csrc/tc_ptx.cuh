@@ -24,10 +24,13 @@ __device__ __forceinline__ void mbar_arrive(uint32_t addr) {
   asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(addr)
                : "memory");
 }
+// One test of the phase; a thread whose phase is not complete is suspended in
+// hardware (up to the 1 ms hint) instead of spinning, so that waiting warps take
+// neither issue slots nor shared-memory bandwidth from the working ones.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(addr), "r"(parity)
@@ -39,14 +42,19 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
   return t;
 }
-// Waits for the phase with the given parity to complete; false after `limit_ns`.
-__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(addr, parity)) return true;
+// The bounded retry loop, kept out of line: the kernels wait in many places and
+// only the first test belongs in their (instruction-cache resident) hot code.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(addr, parity)) {
     if (global_ns() - t0 > limit_ns) return false;
   }
   return true;
+}
+// Waits for the phase with the given parity to complete; false after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(addr, parity)) return true;
+  return mbar_wait_slow(addr, parity, limit_ns);
 }
 
 // Arrives on the mbarrier and raises its expected transaction bytes (TMA).
