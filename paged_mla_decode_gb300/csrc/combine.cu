@@ -76,8 +76,6 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ out_base, in
 // Merge of mla_decode's pieces. One block per (row, head, quarter of the 512 dims):
 // the 8 warps take every 8th piece and each lane 4 consecutive dims, with 4
 // pieces per warp in flight; the warps then add their sums in shared memory.
-// Launched as a programmatic dependent of the decode kernel: its prologue runs
-// while the decode kernel drains, and griddepcontrol.wait orders the reads.
 constexpr int kPieceThreads = 256;
 constexpr int kPieceWarps = kPieceThreads / 32;
 constexpr int kQuarters = 4;
@@ -97,7 +95,6 @@ combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __res
   const int h = (int)(rh - (int64_t)r * heads);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) s_bad = 0;
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");  // decode kernel's writes are visible
   __syncthreads();
   const int np = row_np[r];
   const int base = row_base[r];
@@ -187,18 +184,11 @@ cudaError_t launch_combine_pieces(const DecodeWorkspace& ws, int rows, int heads
                                   int max_pieces_per_row, __nv_bfloat16* out, float* lse,
                                   cudaStream_t stream) {
   (void)max_pieces_per_row;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((int64_t)rows * heads * kQuarters));
-  cfg.blockDim = dim3(kPieceThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_pieces_kernel, ws.row_base, ws.row_np, ws.piece_err,
-                            (const float*)ws.part_lse, (const float*)ws.part_out, heads, out, lse);
+  const unsigned blocks = (unsigned)((int64_t)rows * heads * kQuarters);
+  combine_pieces_kernel<<<blocks, kPieceThreads, 0, stream>>>(
+      ws.row_base, ws.row_np, ws.piece_err, (const float*)ws.part_lse, (const float*)ws.part_out,
+      heads, out, lse);
+  return cudaGetLastError();
 }
 
 }  // namespace mla

@@ -83,8 +83,10 @@ extern "C" mla_status mla_decode(const void* q, const void* kv_pages, int64_t nu
   p.ws.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   p.ws.part_out = reinterpret_cast<float*>(ws + L.part_out);
 
+  if (!p.bf16 && num_pages > (int64_t)(0x7fffffff / kPageSize)) return MLA_ERR_UNSUPPORTED;
+
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode_tensor_core(p, s);
+  cudaError_t e = p.bf16 ? launch_decode_tensor_core(p, s) : launch_decode_fp8(p, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   e = launch_combine_pieces(p.ws, (int)rows, num_heads, G, static_cast<__nv_bfloat16*>(out), lse,
                             s);

@@ -211,8 +211,6 @@ __global__ void __maxnreg__(168)
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (uint32_t)i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // the combine kernel may be scheduled now; it waits for this grid's writes itself
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   // ---- planning (shared by all roles) ----
   __shared__ int64_t s_plan[6];
@@ -294,9 +292,9 @@ __global__ void __maxnreg__(168)
         // page is the tile's page lw / 4). Per tile a lane holds 18 16-byte vectors:
         // vector g*9 + c covers token 8g + lane/4 of the slice, dims 64c + 16 (lane%4)
         // .. +15, so each warp load reads 8 whole 64-byte row pieces. A chunk is
-        // converted as soon as the previous tile's PV has released it, and its
-        // registers are refilled at once with the next tile's bytes: the loads of
-        // tile k+1 are in flight while tile k is multiplied.
+        // converted as soon as the previous tile's PV has released it; once the
+        // whole tile is stored, the registers are refilled with the next tile's
+        // bytes, which are in flight while this tile is multiplied.
         const uint64_t pol = l2_evict_first_policy();
         const int slice0 = 16 * (lw & 3);   // first token of the slice within its page
         const int page_sel = lw >> 2;       // which page of the tile
@@ -383,9 +381,13 @@ __global__ void __maxnreg__(168)
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(bar(BAR_CHUNK_FULL + c));
-            if (have_next) load_slice_chunk(buf, nxt, c);
           }
           if (aborted || !have_next) break;
+          // The next tile's loads go out only after this tile's last proxy fence: a
+          // fence.proxy.async waits for the thread's outstanding loads, so a load
+          // issued between two chunk fences would put its latency in the loop.
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) load_slice_chunk(buf, nxt, c);
           cur = nxt;
         }
       } else {

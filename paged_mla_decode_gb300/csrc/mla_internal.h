@@ -38,6 +38,10 @@ struct DecodeLaunch {
 // Split-KV decode on the tcgen05 tensor cores (decode_tc.cu); heads <= 64.
 cudaError_t launch_decode_tensor_core(const DecodeLaunch& d, cudaStream_t stream);
 
+// Split-KV decode with the e4m3 cache bytes as tensor-core operands
+// (decode_fp8.cu); e4m3 caches only, heads <= 64, num_pages * 64 < 2^31.
+cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream);
+
 // Merge the pieces written by a decode kernel into out (bf16) and lse (fp32).
 cudaError_t launch_combine_pieces(const DecodeWorkspace& ws, int rows, int heads,
                                   int max_pieces_per_row, __nv_bfloat16* out, float* lse,

@@ -44,7 +44,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 // The bounded retry loop, kept out of line: the kernels wait in many places and
 // only the first test belongs in their (instruction-cache resident) hot code.
-__device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parity, uint64_t limit_ns) {
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(addr, parity)) {
     if (global_ns() - t0 > limit_ns) return false;
@@ -73,6 +73,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(mbar)
+      : "memory");
+}
+
+// As tma_load_2d, with an L2 cache policy (createpolicy) for the copied lines.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, int x, int y,
+                                                uint32_t mbar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(mbar), "l"(policy)
       : "memory");
 }
 
@@ -152,6 +162,25 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_taddr, uint64_t a_desc, ui
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A x B, kind::f8f6f4 (8-bit operands, here e4m3; fp32 accumulate),
+// A and B in shared memory.
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_taddr, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_taddr),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// As above with A in TMEM (lane = row, four 8-bit K elements per 32-bit column).
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_taddr),
+      "r"(a_taddr), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives (once) on the mbarrier when all previously issued MMAs of this thread finish.
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
   asm volatile(
@@ -162,22 +191,32 @@ __device__ __forceinline__ void mma_commit(uint32_t mbar) {
 // ---------------------------------------------------------------------------
 // Descriptors
 // ---------------------------------------------------------------------------
-// Shared-memory matrix descriptor, 128-byte swizzle (atoms of 8 rows x 128 B,
-// 16-byte chunk k of row r stored at chunk k ^ (r % 8); atoms 1024-B aligned).
-//   lbo: byte distance between the two 64-element blocks along the contiguous
-//        dimension (MN-major operands spanning more than 64 elements);
+// Shared-memory matrix descriptor.
+//   layout: kSwizzle128 (atoms of 8 rows x 128 B, 16-byte chunk k of row r at
+//           chunk k ^ (r % 8), atoms 1024-B aligned) or kSwizzle64 (8 rows x 64 B,
+//           chunk k of row r at k ^ ((r / 2) % 4), atoms 512-B aligned);
+//   lbo: byte distance between the swizzle-wide blocks along the contiguous
+//        dimension (MN-major operands wider than one block);
 //   sbo: byte distance between consecutive 8-row groups.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+constexpr uint32_t kSwizzle128 = 2;
+constexpr uint32_t kSwizzle64 = 4;
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
-  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  d |= (uint64_t)layout << 61;
   return d;
 }
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return smem_desc(saddr, lbo, sbo, kSwizzle128);
+}
 
-// Instruction descriptor for kind::f16 with fp32 accumulation.
+// Instruction descriptor with fp32 accumulation. For kind::f16 the format codes
+// are f16 = 0 / bf16 = 1; for kind::f8f6f4 code 0 is e4m3, so
+// idesc_f16(m, n, false, ...) also describes e4m3 x e4m3 there.
 //   ab_bf16: operands are bf16 (else f16); a_mn / b_mn: operand is MN-major.
 __host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool ab_bf16, bool a_mn, bool b_mn) {
   return (1u << 4)                                   // D = f32
