@@ -413,8 +413,7 @@ def run_gpu(args):
             "metric": METRIC, "value": kv_gbs, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f16" if kv_dtype == "e4m3" else
-            "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": kv_dtype, "data": "synthetic",
             "config": {"workload": desc, "batch": B, "queries": Q, "heads": H,
                        "seq_lens_total": int(w.seq_lens.sum()), "unique_tokens": w.unique_tokens,
                        "kv_dtype": kv_dtype, "page_size": 64,
@@ -424,7 +423,8 @@ def run_gpu(args):
             "steps_per_s": world * steps_per_s, "tokens_per_s": tokens_per_s,
             "kv_gbs": kv_gbs, "pct_of_hbm_peak": 100.0 * kv_gbs / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 3 * args.steps, "clocks": clocks,
+            # per step: KV append, then q prep (e4m3 caches), decode and combine
+            "gpu_launches": (4 if kv_dtype == "e4m3" else 3) * args.steps, "clocks": clocks,
             "device_status": status,
         }
         print(json.dumps(line), flush=True)

@@ -74,11 +74,12 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ out_base, in
 }
 
 // Merge of mla_decode's pieces. One block per (row, head, quarter of the 512 dims):
-// the 8 warps take every 8th piece and each lane 4 consecutive dims, with 4
+// the 8 warps take every 8th piece and each lane 4 consecutive dims, with 8
 // pieces per warp in flight; the warps then add their sums in shared memory.
 constexpr int kPieceThreads = 256;
 constexpr int kPieceWarps = kPieceThreads / 32;
 constexpr int kQuarters = 4;
+constexpr int kInFlight = 8;  // pieces per warp with loads in flight
 
 __global__ void __launch_bounds__(kPieceThreads)
 combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __restrict__ row_np,
@@ -118,11 +119,11 @@ combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __res
   float wsum = 0.f;
   if (!empty) {
     const int64_t dim0 = 128 * quarter + 4 * lane;
-    for (int s0 = warp; s0 < np; s0 += 4 * kPieceWarps) {
-      float wgt[4];
-      float4 v[4];
+    for (int s0 = warp; s0 < np; s0 += kInFlight * kPieceWarps) {
+      float wgt[kInFlight];
+      float4 v[kInFlight];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kInFlight; ++u) {
         const int s = s0 + u * kPieceWarps;
         wgt[u] = 0.f;
         v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -134,7 +135,7 @@ combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __res
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kInFlight; ++u) {
         if (wgt[u] == 0.f) continue;  // empty piece: its output is never read
         wsum += wgt[u];
         acc.x += wgt[u] * v[u].x;

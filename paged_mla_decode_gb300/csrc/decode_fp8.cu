@@ -12,8 +12,9 @@
 //
 // q (bf16) is scaled per head by a power of two and split into two e4m3 terms
 // q_hi + q_lo, which is exact for bf16 inputs (8 significant bits = 4 + 4), so
-// S_hi + S_lo is q . k up to fp32 accumulation. P = 2^(s - m + 7) is split the
-// same way (8 significant bits, as bf16). All heads attend over the one latent
+// S_hi + S_lo is q . k up to fp32 accumulation. P = 2^(s - m + 6) is split into
+// an e4m3 term and an e5m2 remainder (7 significant bits; the e5m2 range keeps
+// tokens down to 2^-24 of the running maximum). All heads attend over the one latent
 // head ("vLLM x AgentX", section "Kimi K3"), so one page serves 64 heads, and V
 // is read in place through an MN-major descriptor (no distinct values: "How to
 // serve trillions of tokens ...", section "First, understand the workload").
@@ -52,8 +53,8 @@ constexpr int kPageBytes = kPageSize * kDEntry;      // 36864
 constexpr int kLatBlock = kPageSize * 128;           // 8192: 64 rows x 128 dims
 constexpr int kRopeOff = 4 * kLatBlock;              // rope block within a page slot
 constexpr int kPBytes = 64 * 128;                    // P^T: 64 heads x [64 hi | 64 lo]
-constexpr int kPOffset = 7;                          // P = 2^(s - m + 7)
-constexpr float kRescaleThresh = 1.5f;               // P <= 2^8.5 < 448 (e4m3 max)
+constexpr int kPOffset = 6;                          // P = 2^(s - m + 6)
+constexpr float kRescaleThresh = 2.8f;               // P <= 2^8.8 < 448 (e4m3 max)
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 constexpr uint32_t kTmemCols = 512;
@@ -64,29 +65,44 @@ constexpr uint32_t kOCol = 256;
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffPages = 0;
 constexpr int kOffQRope = kOffPages + kRing * kPageBytes;   // 128 rows x 64 B, 64B swizzle
-constexpr int kOffP = kOffQRope + 128 * 64;                 // [2] P^T buffers
-constexpr int kOffAlpha = kOffP + 2 * kPBytes;              // float [2][64]
+constexpr int kPBufs = 3;                                   // P^T buffers (QK runs 2 pages ahead)
+constexpr int kOffP = kOffQRope + 128 * 64;                 // [kPBufs] P^T buffers
+constexpr int kOffAlpha = kOffP + kPBufs * kPBytes;         // float [2][64]
 constexpr int kOffLinv = kOffAlpha + 512;                   // float [64]
 constexpr int kOffFlags = kOffLinv + 256;                   // int [4]
 constexpr int kOffPlan = kOffFlags + 16;                    // int64 [6]
-constexpr int kOffBar = kOffPlan + 48;
+constexpr int kDescRing = 64;                               // page descriptors in flight
+constexpr int kOffDesc = kOffPlan + 48;                     // PageDesc [kDescRing]
+constexpr int kOffBar = kOffDesc + 16 * kDescRing;
 constexpr int BAR_PAGE_FULL = 0;              // [kRing] TMA bytes (or zero fill) landed
 constexpr int BAR_PAGE_EMPTY = kRing;         // [kRing] PV of the slot's page finished
-constexpr int BAR_S_FULL = 2 * kRing;         // [2]
+constexpr int BAR_S_FULL = 2 * kRing;         // [2] page j: buffer j % 2
 constexpr int BAR_S_EMPTY = 2 * kRing + 2;    // [2] (4 softmax warps)
-constexpr int BAR_P_FULL = 2 * kRing + 4;     // [2] (4 softmax warps)
-constexpr int BAR_PV_DONE = 2 * kRing + 6;    // one phase per PV
-constexpr int BAR_O_FULL = 2 * kRing + 7;
-constexpr int BAR_O_EMPTY = 2 * kRing + 8;    // (4 softmax warps)
-constexpr int BAR_Q_READY = 2 * kRing + 9;    // (4 softmax warps)
-constexpr int BAR_Q_EMPTY = 2 * kRing + 10;
-constexpr int BAR_DRAIN = 2 * kRing + 11;
-constexpr int kNumBars = 2 * kRing + 12;
+constexpr int BAR_P_FULL = 2 * kRing + 4;     // [kPBufs] page j: buffer j % 3 (4 softmax warps)
+constexpr int BAR_PV_DONE = 2 * kRing + 7;    // [2] PV of page j commits barrier j % 2
+constexpr int BAR_O_FULL = 2 * kRing + 9;
+constexpr int BAR_O_EMPTY = 2 * kRing + 10;   // (4 softmax warps)
+constexpr int BAR_Q_READY = 2 * kRing + 11;   // (4 softmax warps)
+constexpr int BAR_Q_EMPTY = 2 * kRing + 12;
+constexpr int BAR_DRAIN = 2 * kRing + 13;
+constexpr int kNumBars = 2 * kRing + 14;
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024 alignment
 
 enum Flag { F_ABORT = 0, F_PIECE_BAD = 1 };
+
+// What every role needs to know about the CTA's j-th page, written by the TMA
+// warp (the only planner walker) before it signals the page, read by the MMA and
+// softmax warps after they have waited for it.
+struct PageDesc {
+  int32_t page;    // block-table entry
+  int16_t valid;   // tokens of the row in this page (1..64)
+  int16_t flags;   // kDescPieceStart | kDescPieceEnd | kDescPageOk
+  int32_t row;     // request row r = b * Q + j
+  int32_t slot;    // partial slot of this piece
+};
+constexpr int16_t kDescPieceStart = 1, kDescPieceEnd = 2, kDescPageOk = 4;
 
 struct Fp8Params {
   const __nv_bfloat16* q;
@@ -95,6 +111,7 @@ struct Fp8Params {
   int max_pages;
   const int32_t* seq_lens;
   int batch, nq, heads;
+  int rows;          // batch * nq
   float score_mul;   // sm_scale * log2(e) * kv_scale
   float kv_scale;
   int G;
@@ -114,14 +131,10 @@ struct PageWalker {
   __device__ void settle() {
     if (x < x_end && x == cur.rt + cur.t) cursor_next_row(plan, cur);
   }
-  __device__ bool done() const { return x >= x_end; }
   __device__ int page_in_row() const { return (int)(x - cur.rt); }
   __device__ bool piece_start() const { return x == x_begin || x == cur.rt; }
   __device__ bool piece_end() const { return x + 1 == x_end || x + 1 == cur.rt + cur.t; }
   __device__ int valid_tokens() const { return min(kPageSize, cur.n - page_in_row() * kPageSize); }
-  __device__ int page_id(const int32_t* block_table, int nq, int max_pages) const {
-    return __ldg(block_table + (int64_t)(cur.r / nq) * max_pages + page_in_row());
-  }
   __device__ void next() { ++x; settle(); }
 };
 
@@ -149,17 +162,79 @@ __device__ __forceinline__ float2 e4m3x2_value(uint32_t codes) {
   const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)codes);
   return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
-// hi/lo split of a pair: hi = e4m3(x), lo = e4m3(x - hi); returns the codes of
-// the requested term and (optionally) the represented value hi + lo.
-__device__ __forceinline__ uint32_t split_pair(float x0, float x1, bool want_lo, float2* value) {
-  const uint32_t hi = e4m3x2_of(x0, x1);
-  const float2 hv = e4m3x2_value(hi);
-  const uint32_t lo = e4m3x2_of(x0 - hv.x, x1 - hv.y);
-  if (value) {
-    const float2 lv = e4m3x2_value(lo);
-    *value = make_float2(hv.x + lv.x, hv.y + lv.y);
+// Two floats -> two e5m2 codes (round to nearest even, saturating); `lo` in the low byte.
+__device__ __forceinline__ uint32_t e5m2x2_of(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// q of row blockIdx.x split into the FP8 kernel's A operand, written to copy
+// blockIdx.y. A row t is head 16*(t/32) + t%16, e4m3 term (t/16)%2 (hi, lo); its
+// byte 4i+k is dim 4i+k. The head is scaled by a power of two so that its max |q|
+// lies in [2^7, 2^8), then q_hi = e4m3(q), q_lo = e4m3(q - q_hi): exact for
+// bf16 q (8 significant bits = 4 + 4) down to 2^-10 of the head's max.
+// Four threads per head, 144 dims each.
+__global__ void __launch_bounds__(256)
+    q_prep_kernel(const __nv_bfloat16* __restrict__ q, int rows, int H, float score_mul,
+                  uint8_t* __restrict__ q_prep, float* __restrict__ q_mul) {
+  const int row = blockIdx.x, cp = blockIdx.y;
+  const int h = threadIdx.x >> 2, k4 = threadIdx.x & 3;
+  const bool live = h < H;
+  const uint4* src = reinterpret_cast<const uint4*>(
+      q + ((int64_t)row * H + (live ? h : 0)) * kDEntry + 144 * k4);
+  uint4 w[18];
+#pragma unroll
+  for (int u = 0; u < 18; ++u) w[u] = live ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
+  float amax = 0.f;
+#pragma unroll
+  for (int u = 0; u < 18; ++u) {
+    const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
   }
-  return want_lo ? lo : hi;
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  int shift = 0;
+  if (amax > 0.f && isfinite(amax)) {
+    int e;
+    frexpf(amax, &e);
+    shift = 8 - e;  // scaled max in [2^7, 2^8)
+  }
+  const float sc = live ? ldexpf(1.0f, shift) : 0.f;
+  if (k4 == 0 && cp == 0)
+    q_mul[(int64_t)row * 64 + h] = live ? score_mul * ldexpf(1.0f, -shift) : 0.f;
+  const int t_hi = 32 * (h >> 4) + (h & 15);   // A rows of this head's two terms
+  uint8_t* base = q_prep + ((int64_t)cp * rows + row) * kQPrepRowBytes + 144 * k4;
+  uint4* dst_hi = reinterpret_cast<uint4*>(base + (int64_t)t_hi * kDEntry);
+  uint4* dst_lo = reinterpret_cast<uint4*>(base + (int64_t)(t_hi + 16) * kDEntry);
+#pragma unroll
+  for (int u2 = 0; u2 < 9; ++u2) {  // 16 dims -> one 16-byte vector of each term
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const uint4 wv = w[2 * u2 + half];
+      const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+      uint32_t hc[4], lc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+        const float x0 = f.x * sc, x1 = f.y * sc;
+        hc[k] = e4m3x2_of(x0, x1);
+        const float2 hv = e4m3x2_value(hc[k]);
+        lc[k] = e4m3x2_of(x0 - hv.x, x1 - hv.y);
+      }
+      hw[2 * half] = hc[0] | (hc[1] << 16);
+      hw[2 * half + 1] = hc[2] | (hc[3] << 16);
+      lw[2 * half] = lc[0] | (lc[1] << 16);
+      lw[2 * half + 1] = lc[2] | (lc[3] << 16);
+    }
+    dst_hi[u2] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    dst_lo[u2] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -186,8 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) {
-      const bool by_warps = i == BAR_S_EMPTY || i == BAR_S_EMPTY + 1 || i == BAR_P_FULL ||
-                            i == BAR_P_FULL + 1 || i == BAR_O_EMPTY || i == BAR_Q_READY;
+      const bool by_warps = (i >= BAR_S_EMPTY && i < BAR_S_EMPTY + 2) ||
+                            (i >= BAR_P_FULL && i < BAR_P_FULL + kPBufs) || i == BAR_O_EMPTY ||
+                            i == BAR_Q_READY;
       tc::mbar_init(bar(i), by_warps ? 4 : 1);
     }
     tc::fence_mbar_init();
@@ -227,39 +303,73 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicOr(p.ws.status, MLA_DEVICE_ERR_TIMEOUT);
   };
 
+  const int64_t npages = x_end - x_begin;
+  const PageDesc* desc = reinterpret_cast<const PageDesc*>(smem + kOffDesc);
   if (x_begin < x_end) {
     if (warp == kTmaWarp) {
-      // =================== TMA producer (lane 0) ===================
-      if (lane == 0) {
-        const uint64_t pol = l2_evict_first_policy();
-        PageWalker pw;
-        pw.init(plan, cur0, x_begin, x_end);
-        int64_t j = 0;
-        bool ok = true;
-        for (; !pw.done(); pw.next(), ++j) {
-          const int slot = (int)(j % kRing);
-          const uint32_t round = (uint32_t)(j / kRing);
-          const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
-          if (j >= kRing &&
-              (!tc::mbar_wait(bar(BAR_PAGE_EMPTY + slot), (round - 1) & 1, kWaitNs) ||
-               flags[F_ABORT])) {
-            ok = false;
-            break;
+      // =================== TMA producer ===================
+      // The warp walks the plan 32 pages at a time: lane i takes page j0 + i, so the
+      // 32 block-table reads are in flight together; lane 0 then issues the copies.
+      const uint64_t pol = l2_evict_first_policy();
+      PageDesc* ring = reinterpret_cast<PageDesc*>(smem + kOffDesc);
+      PageWalker pw;
+      pw.init(plan, cur0, x_begin, x_end);
+      int64_t j = 0;
+      bool ok = true;
+      for (int64_t j0 = 0; j0 < npages && ok; j0 += 32) {
+        PageDesc mine{-1, 0, 0, 0, 0};
+        int64_t bt = -1;
+        for (int i = 0; i < 32 && j0 + i < npages; ++i) {
+          if (lane == i) {
+            mine.valid = (int16_t)pw.valid_tokens();
+            mine.flags = (int16_t)((pw.piece_start() ? kDescPieceStart : 0) |
+                                   (pw.piece_end() ? kDescPieceEnd : 0));
+            mine.row = pw.cur.r;
+            mine.slot = pw.cur.base + (c - plan.cta_of(pw.cur.rt));
+            bt = (int64_t)(pw.cur.r / p.nq) * p.max_pages + pw.page_in_row();
           }
-          const int page = pw.page_id(p.block_table, p.nq, p.max_pages);
-          if (page >= 0 && (int64_t)page < p.num_pages) {
-            tc::mbar_arrive_expect_tx(bar(BAR_PAGE_FULL + slot), (uint32_t)kPageBytes);
-            const int y = page * kPageSize;
+          pw.next();
+        }
+        if (bt >= 0) {
+          mine.page = __ldg(p.block_table + bt);
+          if (mine.page >= 0 && (int64_t)mine.page < p.num_pages) mine.flags |= kDescPageOk;
+          ring[(j0 + lane) % kDescRing] = mine;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          for (; j < j0 + 32 && j < npages; ++j) {
+            const PageDesc d = ring[j % kDescRing];
+            const int slot = (int)(j % kRing);
+            const uint32_t round = (uint32_t)(j / kRing);
+            const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
+            if (j >= kRing &&
+                (!tc::mbar_wait(bar(BAR_PAGE_EMPTY + slot), (round - 1) & 1, kWaitNs) ||
+                 flags[F_ABORT])) {
+              ok = false;
+              break;
+            }
+            if (d.flags & kDescPieceStart)  // the softmax warps read this row's q soon
+              tc::prefetch_l2_bulk(
+                  p.ws.q_prep + ((int64_t)(c % p.ws.q_copies) * p.rows + d.row) * kQPrepRowBytes,
+                  (uint32_t)kQPrepRowBytes);
+            if (d.flags & kDescPageOk) {
+              tc::mbar_arrive_expect_tx(bar(BAR_PAGE_FULL + slot), (uint32_t)kPageBytes);
+              const int y = d.page * kPageSize;
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-              tc::tma_load_2d_hint(page_base + b * kLatBlock, &lat_map, 128 * b, y,
+              for (int b = 0; b < 4; ++b)
+                tc::tma_load_2d_hint(page_base + b * kLatBlock, &lat_map, 128 * b, y,
+                                     bar(BAR_PAGE_FULL + slot), pol);
+              tc::tma_load_2d_hint(page_base + kRopeOff, &rope_map, kDLatent, y,
                                    bar(BAR_PAGE_FULL + slot), pol);
-            tc::tma_load_2d_hint(page_base + kRopeOff, &rope_map, kDLatent, y,
-                                 bar(BAR_PAGE_FULL + slot), pol);
-          } else {
-            tc::mbar_arrive(bar(BAR_PAGE_FULL + slot));  // bad id: the MMA warp zero-fills
+            } else {
+              tc::mbar_arrive(bar(BAR_PAGE_FULL + slot));  // bad id: the MMA warp zero-fills
+            }
           }
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        j = __shfl_sync(0xffffffffu, j, 0);
+      }
+      if (lane == 0) {
         if (!ok) abort_cta();
         // no copy may land after the CTA exits: wait for the last issued pages
         for (int64_t jj = j > kRing ? j - kRing : 0; jj < j; ++jj)
@@ -269,32 +379,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // =================== MMA issuer (lane 0; the warp zero-fills) ===================
-      constexpr uint32_t id_qk = tc::idesc_f16(128, 64, false, false, false);
-      constexpr uint32_t id_pv = tc::idesc_f16(128, 64, false, true, false);
+      constexpr uint32_t id_qk = tc::idesc_f8(128, 64, tc::kFmtE4M3, tc::kFmtE4M3, false, false);
+      // PV: A = V^T (e4m3, MN-major); B = P^T hi (e4m3) or lo (e5m2), K-major
+      constexpr uint32_t id_pv_hi = tc::idesc_f8(128, 64, tc::kFmtE4M3, tc::kFmtE4M3, true, false);
+      constexpr uint32_t id_pv_lo = tc::idesc_f8(128, 64, tc::kFmtE4M3, tc::kFmtE5M2, true, false);
       const uint64_t qrope_desc = tc::smem_desc(sbase + kOffQRope, 16, 512, tc::kSwizzle64);
       const bool leader = lane == 0;
-      // bounded wait by lane 0, result shared with the warp
-      auto wait0 = [&](int b, uint32_t parity) -> bool {
-        bool got = true;
-        if (leader) got = tc::mbar_wait(bar(b), parity, kWaitNs);
-        return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-      };
       bool ok = true;
       int q_piece = 0, o_piece = 0;
-      struct Prev { int64_t j; int slot; bool ps, pe; } prev{0, 0, false, false};
-      bool have_prev = false;
-      auto pv = [&](const Prev& pr) -> bool {
-        if (!wait0(BAR_P_FULL + (int)(pr.j & 1), (uint32_t)(pr.j >> 1) & 1)) return false;
-        if (pr.ps) {
-          if (o_piece > 0 && !wait0(BAR_O_EMPTY, (uint32_t)(o_piece - 1) & 1)) return false;
-          ++o_piece;
-        }
+      // PV of page k: O^T += V^T P^T (P(k) and, at a piece start, O_EMPTY are ready)
+      auto pv_issue = [&](int64_t k) {
+        const int pb_i = (int)(k % kPBufs);
+        const PageDesc d = desc[k % kDescRing];
+        const bool ps = d.flags & kDescPieceStart, pe = d.flags & kDescPieceEnd;
+        if (ps) ++o_piece;
+        const int slot = (int)(k % kRing);
         if (leader) {
           tc::fence_after_sync();
-          const uint32_t page_base = sbase + kOffPages + pr.slot * kPageBytes;
+          const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
           const uint64_t va = tc::smem_desc(page_base, kLatBlock, 1024, tc::kSwizzle128);
-          const uint64_t pb =
-              tc::smem_desc(sbase + kOffP + (int)(pr.j & 1) * kPBytes, 16, 1024, tc::kSwizzle128);
+          const uint64_t pb = tc::smem_desc(sbase + kOffP + pb_i * kPBytes, 16, 1024, tc::kSwizzle128);
 #pragma unroll
           for (int blk = 0; blk < 4; ++blk)
 #pragma unroll
@@ -303,44 +407,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int part = 0; part < 2; ++part)
                 tc::mma_f8_ss(tmem + kOCol + 64 * blk,
                               va + (uint64_t)((blk * kLatBlock + s * 4096) >> 4),
-                              pb + (uint64_t)((64 * part + 32 * s) >> 4), id_pv,
-                              !(pr.ps && s == 0 && part == 0));
-          tc::mma_commit(bar(BAR_PAGE_EMPTY + pr.slot));
-          tc::mma_commit(bar(BAR_PV_DONE));
-          if (pr.pe) tc::mma_commit(bar(BAR_O_FULL));
+                              pb + (uint64_t)((64 * part + 32 * s) >> 4),
+                              part ? id_pv_lo : id_pv_hi, !(ps && s == 0 && part == 0));
+          tc::mma_commit(bar(BAR_PAGE_EMPTY + slot));
+          tc::mma_commit(bar(BAR_PV_DONE + (int)(k & 1)));
+          if (pe) tc::mma_commit(bar(BAR_O_FULL));
         }
         __syncwarp();
-        return true;
       };
-      PageWalker pw;
-      pw.init(plan, cur0, x_begin, x_end);
-      for (int64_t j = 0; !pw.done() && ok; pw.next(), ++j) {
-        if (flags[F_ABORT]) {
-          ok = false;
-          break;
-        }
-        const bool ps = pw.piece_start(), pe = pw.piece_end();
-        const int slot = (int)(j % kRing);
+      // QK of page k: S = A . page^T (latent part of A from TMEM, rope from shared
+      // memory); page k, its S buffer and (at a piece start) its q are ready
+      auto qk_issue = [&](int64_t k, const PageDesc& d) {
+        const int slot = (int)(k % kRing);
         const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
-        // a piece's first QK needs its q, staged after the previous piece's output
-        if (ps && have_prev) {
-          ok = pv(prev);
-          have_prev = false;
-          if (!ok) break;
-        }
-        if (ps) {
-          ok = wait0(BAR_Q_READY, (uint32_t)q_piece & 1);
-          ++q_piece;
-          if (!ok) break;
-        }
-        ok = wait0(BAR_PAGE_FULL + slot, (uint32_t)(j / kRing) & 1);
-        if (ok && j >= 2) ok = wait0(BAR_S_EMPTY + (int)(j & 1), (uint32_t)((j >> 1) - 1) & 1);
-        if (!ok) break;
+        if (d.flags & kDescPieceStart) ++q_piece;
         // rows past the page's last token (all rows of a bad page id) become zeros,
         // so that masked tokens contribute 0 * finite to PV
-        const int page = pw.page_id(p.block_table, p.nq, p.max_pages);
-        const bool page_ok = page >= 0 && (int64_t)page < p.num_pages;
-        const int zero_from = page_ok ? pw.valid_tokens() : 0;
+        const int zero_from = (d.flags & kDescPageOk) ? d.valid : 0;
         if (zero_from < kPageSize) {
           for (int i = lane; i < (kPageSize - zero_from) * 36; i += 32) {
             const int row = zero_from + i / 36, u = i % 36;
@@ -353,10 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (leader) {
           tc::fence_after_sync();
-          // ---- S = A . page^T: latent part of A from TMEM, rope part from shared memory ----
           const uint64_t kb = tc::smem_desc(page_base, 16, 1024, tc::kSwizzle128);
           const uint64_t rb = tc::smem_desc(page_base + kRopeOff, 16, 512, tc::kSwizzle64);
-          const uint32_t d_s = tmem + s_col((int)(j & 1));
+          const uint32_t d_s = tmem + s_col((int)(k & 1));
 #pragma unroll
           for (int s = 0; s < 16; ++s)
             tc::mma_f8_ts(d_s, tmem + kQCol + 8 * s,
@@ -365,19 +447,61 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < 2; ++s)
             tc::mma_f8_ss(d_s, qrope_desc + (uint64_t)((32 * s) >> 4),
                           rb + (uint64_t)((32 * s) >> 4), id_qk, 1);
-          tc::mma_commit(bar(BAR_S_FULL + (int)(j & 1)));
-          if (pe) tc::mma_commit(bar(BAR_Q_EMPTY));
+          tc::mma_commit(bar(BAR_S_FULL + (int)(k & 1)));
+          if (d.flags & kDescPieceEnd) tc::mma_commit(bar(BAR_Q_EMPTY));
         }
         __syncwarp();
-        // ---- O^T += V^T P^T of the previous page ----
-        if (have_prev) {
-          ok = pv(prev);
-          if (!ok) break;
+      };
+      // Lane 0 polls the barriers and issues whatever is ready, PV first (it frees a
+      // ring slot), else the next QK. QK runs up to two pages ahead of PV (two S
+      // buffers, three P buffers); a piece's first QK waits until every PV of the
+      // previous piece is issued, since its q is staged after that piece's output
+      // has been read. The loop gives up when nothing has been ready for kWaitNs.
+      int64_t qk_next = 0, pv_next = 0;
+      uint64_t idle_since = tc::global_ns();
+      while (pv_next < npages) {
+        int action = 0;  // 1: PV(pv_next), 2: QK(qk_next)
+        if (leader) {
+          if (flags[F_ABORT]) {
+            action = -1;
+          } else if (pv_next < qk_next &&
+                     tc::mbar_test(bar(BAR_P_FULL + (int)(pv_next % kPBufs)),
+                                   (uint32_t)(pv_next / kPBufs) & 1)) {
+            const PageDesc d = desc[pv_next % kDescRing];
+            if (!(d.flags & kDescPieceStart) || o_piece == 0 ||
+                tc::mbar_test(bar(BAR_O_EMPTY), (uint32_t)(o_piece - 1) & 1))
+              action = 1;
+          }
+          if (action == 0 && qk_next < npages && qk_next <= pv_next + 2 &&
+              tc::mbar_test(bar(BAR_PAGE_FULL + (int)(qk_next % kRing)),
+                            (uint32_t)(qk_next / kRing) & 1)) {
+            const PageDesc d = desc[qk_next % kDescRing];
+            const bool ps = d.flags & kDescPieceStart;
+            if ((!ps || (pv_next == qk_next &&
+                         tc::mbar_test(bar(BAR_Q_READY), (uint32_t)q_piece & 1))) &&
+                (qk_next < 2 || tc::mbar_test(bar(BAR_S_EMPTY + (int)(qk_next & 1)),
+                                              (uint32_t)((qk_next >> 1) - 1) & 1)))
+              action = 2;
+          }
+          if (action == 0) {
+            if (tc::global_ns() - idle_since > kWaitNs) action = -1;
+          } else {
+            idle_since = tc::global_ns();
+          }
         }
-        prev = Prev{j, slot, ps, pe};
-        have_prev = true;
+        action = __shfl_sync(0xffffffffu, action, 0);
+        if (action < 0) {
+          ok = false;
+          break;
+        }
+        if (action == 1) {
+          pv_issue(pv_next);
+          ++pv_next;
+        } else if (action == 2) {
+          qk_issue(qk_next, desc[qk_next % kDescRing]);
+          ++qk_next;
+        }
       }
-      if (ok && have_prev) ok = pv(prev);
       if (leader) {
         if (!ok) abort_cta();
         // drain: every issued MMA has finished before TMEM is freed
@@ -394,10 +518,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY, l = 0.f, qmul = 0.f;
       int piece = 0;
       bool ok = true;
-      PageWalker pw;
-      pw.init(plan, cur0, x_begin, x_end);
-      for (int64_t j = 0; !pw.done(); pw.next(), ++j) {
-        const bool ps = pw.piece_start(), pe = pw.piece_end();
+      for (int64_t j = 0; j < npages; ++j) {
+        // Page 0 opens the first piece, whose row the plan gives: its q is staged at
+        // once. Later pages' descriptors are read once the page has landed.
+        int row = cur0.r;
+        bool ps = j == 0;
+        if (j > 0) {
+          const bool got = tc::mbar_wait(bar(BAR_PAGE_FULL + (int)(j % kRing)),
+                                         (uint32_t)(j / kRing) & 1, kWaitNs);
+          if (named_bar_softmax_or(!got || flags[F_ABORT])) {
+            ok = false;
+            break;
+          }
+          const PageDesc d0 = desc[j % kDescRing];
+          row = d0.row;
+          ps = d0.flags & kDescPieceStart;
+        }
         if (ps) {
           // ---- stage q of this row: per-head power-of-two scale, e4m3 hi/lo split ----
           if (piece > 0) {
@@ -407,84 +543,37 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
           }
-          const bool live = h < H;
-          const uint4* qrow = reinterpret_cast<const uint4*>(
-              p.q + ((int64_t)pw.cur.r * H + (live ? h : 0)) * kDEntry);
-          float amax = 0.f;
-          if (live) {
-#pragma unroll 4
-            for (int u = 0; u < kDEntry / 8; ++u) {
-              const uint4 w = __ldg(qrow + u);
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          // the prepared row of this thread's lane (copy chosen by CTA index)
+          const uint4* src = reinterpret_cast<const uint4*>(
+              p.ws.q_prep + (((int64_t)(c % p.ws.q_copies) * p.rows + row) * 128 + t) * kDEntry);
+          uint4 w[36];
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
-                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-              }
-            }
-          }
-          int shift = 0;
-          if (amax > 0.f && isfinite(amax)) {
-            int e;
-            frexpf(amax, &e);
-            shift = 8 - e;  // scaled max in [2^7, 2^8)
-          }
-          const float sc = live ? ldexpf(1.0f, shift) : 0.f;
-          qmul = live ? p.score_mul * ldexpf(1.0f, -shift) : 0.f;
-          // latent dims: TMEM columns, four e4m3 codes each
-#pragma unroll 1
+          for (int u = 0; u < 36; ++u) w[u] = __ldg(src + u);
+          qmul = h < H ? __ldg(p.ws.q_mul + (int64_t)row * 64 + h) : 0.f;
+#pragma unroll
           for (int blk = 0; blk < 4; ++blk) {
             uint32_t r[32];
 #pragma unroll
-            for (int c8 = 0; c8 < 16; ++c8) {
-              const uint4 w = __ldg(qrow + blk * 16 + c8);
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-              uint32_t codes[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
-                codes[k] = split_pair(f.x * sc, f.y * sc, part != 0, nullptr);
-              }
-              r[2 * c8] = codes[0] | (codes[1] << 16);
-              r[2 * c8 + 1] = codes[2] | (codes[3] << 16);
+            for (int u = 0; u < 8; ++u) {
+              r[4 * u] = w[8 * blk + u].x;
+              r[4 * u + 1] = w[8 * blk + u].y;
+              r[4 * u + 2] = w[8 * blk + u].z;
+              r[4 * u + 3] = w[8 * blk + u].w;
             }
             tc::tmem_st32(tmem + lane_base + kQCol + 32 * blk, r);
           }
-          // rope dims: shared memory row t (64 B, 64-byte swizzle)
+          // rope words: shared memory row t (64 B, 64-byte swizzle)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            uint32_t r4[4];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              const uint4 w = __ldg(qrow + 64 + 2 * u + half);
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-              uint32_t codes[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
-                codes[k] = split_pair(f.x * sc, f.y * sc, part != 0, nullptr);
-              }
-              r4[2 * half] = codes[0] | (codes[1] << 16);
-              r4[2 * half + 1] = codes[2] | (codes[3] << 16);
-            }
             const uint32_t a = sbase + kOffQRope + t * 64 + ((u ^ ((t >> 1) & 3)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(r4[0]),
-                         "r"(r4[1]), "r"(r4[2]), "r"(r4[3]));
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(w[32 + u].x),
+                         "r"(w[32 + u].y), "r"(w[32 + u].z), "r"(w[32 + u].w));
           }
           tc::tmem_wait_st();
           tc::fence_proxy_async_smem();
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(bar(BAR_Q_READY));
-        }
-        // page validity (tokens of a bad page id are masked and reported)
-        const int valid = pw.valid_tokens();
-        const int page = pw.page_id(p.block_table, p.nq, p.max_pages);
-        const bool page_ok = page >= 0 && (int64_t)page < p.num_pages;
-        const int nvis = page_ok ? valid : 0;
-        if (t == 0 && valid > 0 && !page_ok) {
-          flags[F_PIECE_BAD] = 1;
-          atomicOr(p.ws.status, MLA_DEVICE_ERR_BAD_PAGE);
         }
         // ---- S of this page ----
         {
@@ -494,6 +583,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+        }
+        // page validity (tokens of a bad page id are masked and reported)
+        const PageDesc d = desc[j % kDescRing];
+        const bool pe = d.flags & kDescPieceEnd;
+        const bool page_ok = d.flags & kDescPageOk;
+        const int nvis = page_ok ? d.valid : 0;
+        if (t == 0 && !page_ok) {
+          flags[F_PIECE_BAD] = 1;
+          atomicOr(p.ws.status, MLA_DEVICE_ERR_BAD_PAGE);
         }
         tc::fence_after_sync();
         float v[64];
@@ -540,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (named_bar_softmax_or(grow)) {
           // rare: bring O^T (PV of the previous page done) to the new maxima
           const bool got =
-              tc::mbar_wait(bar(BAR_PV_DONE), (uint32_t)(j - 1) & 1, kWaitNs);
+              tc::mbar_wait(bar(BAR_PV_DONE + (int)((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1,
+                            kWaitNs);
           if (named_bar_softmax_or(!got)) {
             ok = false;
             break;
@@ -562,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc::tmem_wait_st();
         }
-        // ---- P = 2^(s - m + 7) as e4m3 hi + lo, row h of P^T ----
+        // ---- P = 2^(s - m + 6) as e4m3 hi + e5m2 lo, row h of P^T ----
         {
           const float mu = m == -INFINITY ? 0.f : m - (float)kPOffset;
           uint32_t hw[8], lw[8];
@@ -576,9 +675,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float p0 = fast_exp2(s[i] - mu), p1 = fast_exp2(s[i + 1] - mu);
               const uint32_t hc = e4m3x2_of(p0, p1);
               const float2 hv = e4m3x2_value(hc);
-              const uint32_t lc = e4m3x2_of(p0 - hv.x, p1 - hv.y);
-              const float2 lv = e4m3x2_value(lc);
-              rs += (hv.x + lv.x) + (hv.y + lv.y);
+              const uint32_t lc = e5m2x2_of(p0 - hv.x, p1 - hv.y);
+              rs += p0 + p1;  // the exact P: lse does not carry the operand rounding
               hcode[e] = hc;
               lcode[e] = lc;
             }
@@ -587,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           rs += __shfl_xor_sync(0xffffffffu, rs, 16);
           l += rs;
-          const uint32_t prow = sbase + kOffP + (int)(j & 1) * kPBytes + h * 128;
+          const uint32_t prow = sbase + kOffP + (int)(j % kPBufs) * kPBytes + h * 128;
           const int sw = h & 7;
 #pragma unroll
           for (int q2 = 0; q2 < 2; ++q2) {
@@ -602,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(bar(BAR_P_FULL + (int)(j & 1)));
+        if (lane == 0) tc::mbar_arrive(bar(BAR_P_FULL + (int)(j % kPBufs)));
         if (pe) {
           // ---- epilogue: O^T / l -> this piece's partial slot ----
           {
@@ -613,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tc::fence_after_sync();
-          const int slot = pw.cur.base + (c - plan.cta_of(pw.cur.rt));
+          const int slot = d.slot;
           if (part == 0) {
             linv_s[h] = l > 0.f ? p.kv_scale / l : 0.f;
             if (h < H)
@@ -663,6 +761,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+cudaError_t launch_q_prep(const __nv_bfloat16* q, int rows, int heads, float score_mul,
+                          const DecodeWorkspace& ws, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  q_prep_kernel<<<dim3((unsigned)rows, (unsigned)ws.q_copies), 256, 0, stream>>>(
+      q, rows, heads, score_mul, ws.q_prep, ws.q_mul);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
   static std::atomic<int> configured[64];
   int dev = 0;
@@ -708,6 +814,7 @@ cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
   p.batch = d.batch;
   p.nq = d.nq;
   p.heads = d.heads;
+  p.rows = d.batch * d.nq;
   p.score_mul = d.score_mul;
   p.kv_scale = d.kv_scale;
   p.G = d.G;
