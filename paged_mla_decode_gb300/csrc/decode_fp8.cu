@@ -19,15 +19,16 @@
 // is read in place through an MN-major descriptor (no distinct values: "How to
 // serve trillions of tokens ...", section "First, understand the workload").
 //
-// Warp roles (192 threads):
+// Warp roles (224 threads):
 //   warps 0-3  q staging, softmax and epilogue. Thread t owns TMEM lane t: row t
 //              of A and S is (head 16*(t/32) + t%16, part (t/16)%2), part 0 = hi,
 //              1 = lo, so the two terms of a head meet inside one warp; for O^T
 //              lane t is dim t of each 128-dim block.
 //   warp 4     TMA producer: pages into a ring of kRing shared-memory slots
 //              (128-byte swizzled latent blocks, 64-byte swizzled rope block).
-//   warp 5     TMEM allocation and the thread that issues every tcgen05.mma; the
-//              warp zeroes the rows of a partial page past its last token first.
+//   warp 5     TMEM allocation; issues QK (lane 0) after zeroing the rows of a
+//              partial page past its last token.
+//   warp 6     issues PV (lane 0).
 // TMEM (512 columns): A latent part [0,128), S buffers [128,192) [192,256),
 // O^T [256,512). The rope part of A is in shared memory.
 //
@@ -45,9 +46,10 @@
 namespace mla {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kQkWarp = 5;   // allocates TMEM, issues QK
+constexpr int kPvWarp = 6;   // issues PV
 constexpr int kRing = 5;                             // pages in flight
 constexpr int kPageBytes = kPageSize * kDEntry;      // 36864
 constexpr int kLatBlock = kPageSize * 128;           // 8192: 64 rows x 128 dims
@@ -84,8 +86,9 @@ constexpr int BAR_O_FULL = 2 * kRing + 9;
 constexpr int BAR_O_EMPTY = 2 * kRing + 10;   // (4 softmax warps)
 constexpr int BAR_Q_READY = 2 * kRing + 11;   // (4 softmax warps)
 constexpr int BAR_Q_EMPTY = 2 * kRing + 12;
-constexpr int BAR_DRAIN = 2 * kRing + 13;
-constexpr int kNumBars = 2 * kRing + 14;
+constexpr int BAR_DRAIN = 2 * kRing + 13;      // [2] QK warp, PV warp
+constexpr int BAR_P_EMPTY = 2 * kRing + 15;    // [kPBufs] PV of page j read P buffer j % 3
+constexpr int kNumBars = 2 * kRing + 15 + kPBufs;
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024 alignment
@@ -270,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     flags[F_ABORT] = 0;
     flags[F_PIECE_BAD] = 0;
   }
-  if (warp == kMmaWarp) {
+  if (warp == kQkWarp) {
     tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc::tmem_relinquish();
   }
@@ -377,136 +380,124 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kWaitNs);
       }
       __syncwarp();
-    } else if (warp == kMmaWarp) {
-      // =================== MMA issuer (lane 0; the warp zero-fills) ===================
+    } else if (warp == kQkWarp || warp == kPvWarp) {
+      // ============ MMA issuers: QK warp and PV warp, lane 0 issues ============
+      // The two streams are issued by different threads, so neither's completion
+      // implies the other's: P buffer reuse and the O^T rescale wait on the PV
+      // warp's own commits (P_EMPTY, PV_DONE).
       constexpr uint32_t id_qk = tc::idesc_f8(128, 64, tc::kFmtE4M3, tc::kFmtE4M3, false, false);
       // PV: A = V^T (e4m3, MN-major); B = P^T hi (e4m3) or lo (e5m2), K-major
       constexpr uint32_t id_pv_hi = tc::idesc_f8(128, 64, tc::kFmtE4M3, tc::kFmtE4M3, true, false);
       constexpr uint32_t id_pv_lo = tc::idesc_f8(128, 64, tc::kFmtE4M3, tc::kFmtE5M2, true, false);
-      const uint64_t qrope_desc = tc::smem_desc(sbase + kOffQRope, 16, 512, tc::kSwizzle64);
       const bool leader = lane == 0;
+      // bounded wait by lane 0, result shared with the warp
+      auto wait0 = [&](int b, uint32_t parity) -> bool {
+        bool got = true;
+        if (leader) got = tc::mbar_wait(bar(b), parity, kWaitNs);
+        return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+      };
       bool ok = true;
-      int q_piece = 0, o_piece = 0;
-      // PV of page k: O^T += V^T P^T (P(k) and, at a piece start, O_EMPTY are ready)
-      auto pv_issue = [&](int64_t k) {
-        const int pb_i = (int)(k % kPBufs);
-        const PageDesc d = desc[k % kDescRing];
-        const bool ps = d.flags & kDescPieceStart, pe = d.flags & kDescPieceEnd;
-        if (ps) ++o_piece;
-        const int slot = (int)(k % kRing);
-        if (leader) {
-          tc::fence_after_sync();
+      if (warp == kQkWarp) {
+        const uint64_t qrope_desc = tc::smem_desc(sbase + kOffQRope, 16, 512, tc::kSwizzle64);
+        int q_piece = 0;
+        for (int64_t k = 0; k < npages && ok; ++k) {
+          if (flags[F_ABORT]) {
+            ok = false;
+            break;
+          }
+          const int slot = (int)(k % kRing);
           const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
-          const uint64_t va = tc::smem_desc(page_base, kLatBlock, 1024, tc::kSwizzle128);
-          const uint64_t pb = tc::smem_desc(sbase + kOffP + pb_i * kPBytes, 16, 1024, tc::kSwizzle128);
+          ok = wait0(BAR_PAGE_FULL + slot, (uint32_t)(k / kRing) & 1);
+          if (!ok) break;
+          const PageDesc d = desc[k % kDescRing];
+          if (d.flags & kDescPieceStart) {
+            ok = wait0(BAR_Q_READY, (uint32_t)q_piece & 1);
+            ++q_piece;
+          }
+          if (ok && k >= 2) ok = wait0(BAR_S_EMPTY + (int)(k & 1), (uint32_t)((k >> 1) - 1) & 1);
+          if (!ok) break;
+          // rows past the page's last token (all rows of a bad page id) become zeros,
+          // so that masked tokens contribute 0 * finite to PV
+          const int zero_from = (d.flags & kDescPageOk) ? d.valid : 0;
+          if (zero_from < kPageSize) {
+            for (int i = lane; i < (kPageSize - zero_from) * 36; i += 32) {
+              const int row = zero_from + i / 36, u = i % 36;
+              const uint32_t a = u < 32 ? page_base + (u >> 3) * kLatBlock + row * 128 + (u & 7) * 16
+                                        : page_base + kRopeOff + row * 64 + (u - 32) * 16;
+              asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(a), "r"(0u));
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+          }
+          if (leader) {
+            // ---- S = A . page^T: latent part of A from TMEM, rope from shared memory ----
+            tc::fence_after_sync();
+            const uint64_t kb = tc::smem_desc(page_base, 16, 1024, tc::kSwizzle128);
+            const uint64_t rb = tc::smem_desc(page_base + kRopeOff, 16, 512, tc::kSwizzle64);
+            const uint32_t d_s = tmem + s_col((int)(k & 1));
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk)
+            for (int s = 0; s < 16; ++s)
+              tc::mma_f8_ts(d_s, tmem + kQCol + 8 * s,
+                            kb + (uint64_t)(((s >> 2) * kLatBlock + (s & 3) * 32) >> 4), id_qk,
+                            s > 0);
 #pragma unroll
             for (int s = 0; s < 2; ++s)
-#pragma unroll
-              for (int part = 0; part < 2; ++part)
-                tc::mma_f8_ss(tmem + kOCol + 64 * blk,
-                              va + (uint64_t)((blk * kLatBlock + s * 4096) >> 4),
-                              pb + (uint64_t)((64 * part + 32 * s) >> 4),
-                              part ? id_pv_lo : id_pv_hi, !(ps && s == 0 && part == 0));
-          tc::mma_commit(bar(BAR_PAGE_EMPTY + slot));
-          tc::mma_commit(bar(BAR_PV_DONE + (int)(k & 1)));
-          if (pe) tc::mma_commit(bar(BAR_O_FULL));
-        }
-        __syncwarp();
-      };
-      // QK of page k: S = A . page^T (latent part of A from TMEM, rope from shared
-      // memory); page k, its S buffer and (at a piece start) its q are ready
-      auto qk_issue = [&](int64_t k, const PageDesc& d) {
-        const int slot = (int)(k % kRing);
-        const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
-        if (d.flags & kDescPieceStart) ++q_piece;
-        // rows past the page's last token (all rows of a bad page id) become zeros,
-        // so that masked tokens contribute 0 * finite to PV
-        const int zero_from = (d.flags & kDescPageOk) ? d.valid : 0;
-        if (zero_from < kPageSize) {
-          for (int i = lane; i < (kPageSize - zero_from) * 36; i += 32) {
-            const int row = zero_from + i / 36, u = i % 36;
-            const uint32_t a = u < 32 ? page_base + (u >> 3) * kLatBlock + row * 128 + (u & 7) * 16
-                                      : page_base + kRopeOff + row * 64 + (u - 32) * 16;
-            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(a), "r"(0u));
+              tc::mma_f8_ss(d_s, qrope_desc + (uint64_t)((32 * s) >> 4),
+                            rb + (uint64_t)((32 * s) >> 4), id_qk, 1);
+            tc::mma_commit(bar(BAR_S_FULL + (int)(k & 1)));
+            if (d.flags & kDescPieceEnd) tc::mma_commit(bar(BAR_Q_EMPTY));
           }
-          tc::fence_proxy_async_smem();
           __syncwarp();
         }
-        if (leader) {
-          tc::fence_after_sync();
-          const uint64_t kb = tc::smem_desc(page_base, 16, 1024, tc::kSwizzle128);
-          const uint64_t rb = tc::smem_desc(page_base + kRopeOff, 16, 512, tc::kSwizzle64);
-          const uint32_t d_s = tmem + s_col((int)(k & 1));
-#pragma unroll
-          for (int s = 0; s < 16; ++s)
-            tc::mma_f8_ts(d_s, tmem + kQCol + 8 * s,
-                          kb + (uint64_t)(((s >> 2) * kLatBlock + (s & 3) * 32) >> 4), id_qk, s > 0);
-#pragma unroll
-          for (int s = 0; s < 2; ++s)
-            tc::mma_f8_ss(d_s, qrope_desc + (uint64_t)((32 * s) >> 4),
-                          rb + (uint64_t)((32 * s) >> 4), id_qk, 1);
-          tc::mma_commit(bar(BAR_S_FULL + (int)(k & 1)));
-          if (d.flags & kDescPieceEnd) tc::mma_commit(bar(BAR_Q_EMPTY));
-        }
-        __syncwarp();
-      };
-      // Lane 0 polls the barriers and issues whatever is ready, PV first (it frees a
-      // ring slot), else the next QK. QK runs up to two pages ahead of PV (two S
-      // buffers, three P buffers); a piece's first QK waits until every PV of the
-      // previous piece is issued, since its q is staged after that piece's output
-      // has been read. The loop gives up when nothing has been ready for kWaitNs.
-      int64_t qk_next = 0, pv_next = 0;
-      uint64_t idle_since = tc::global_ns();
-      while (pv_next < npages) {
-        int action = 0;  // 1: PV(pv_next), 2: QK(qk_next)
-        if (leader) {
+      } else {
+        int o_piece = 0;
+        for (int64_t k = 0; k < npages && ok; ++k) {
           if (flags[F_ABORT]) {
-            action = -1;
-          } else if (pv_next < qk_next &&
-                     tc::mbar_test(bar(BAR_P_FULL + (int)(pv_next % kPBufs)),
-                                   (uint32_t)(pv_next / kPBufs) & 1)) {
-            const PageDesc d = desc[pv_next % kDescRing];
-            if (!(d.flags & kDescPieceStart) || o_piece == 0 ||
-                tc::mbar_test(bar(BAR_O_EMPTY), (uint32_t)(o_piece - 1) & 1))
-              action = 1;
+            ok = false;
+            break;
           }
-          if (action == 0 && qk_next < npages && qk_next <= pv_next + 2 &&
-              tc::mbar_test(bar(BAR_PAGE_FULL + (int)(qk_next % kRing)),
-                            (uint32_t)(qk_next / kRing) & 1)) {
-            const PageDesc d = desc[qk_next % kDescRing];
-            const bool ps = d.flags & kDescPieceStart;
-            if ((!ps || (pv_next == qk_next &&
-                         tc::mbar_test(bar(BAR_Q_READY), (uint32_t)q_piece & 1))) &&
-                (qk_next < 2 || tc::mbar_test(bar(BAR_S_EMPTY + (int)(qk_next & 1)),
-                                              (uint32_t)((qk_next >> 1) - 1) & 1)))
-              action = 2;
+          const int pb_i = (int)(k % kPBufs);
+          ok = wait0(BAR_P_FULL + pb_i, (uint32_t)(k / kPBufs) & 1);
+          if (!ok) break;
+          const PageDesc d = desc[k % kDescRing];
+          const bool ps = d.flags & kDescPieceStart, pe = d.flags & kDescPieceEnd;
+          if (ps) {
+            if (o_piece > 0) ok = wait0(BAR_O_EMPTY, (uint32_t)(o_piece - 1) & 1);
+            ++o_piece;
+            if (!ok) break;
           }
-          if (action == 0) {
-            if (tc::global_ns() - idle_since > kWaitNs) action = -1;
-          } else {
-            idle_since = tc::global_ns();
+          if (leader) {
+            // ---- O^T += V^T P^T ----
+            tc::fence_after_sync();
+            const int slot = (int)(k % kRing);
+            const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
+            const uint64_t va = tc::smem_desc(page_base, kLatBlock, 1024, tc::kSwizzle128);
+            const uint64_t pb =
+                tc::smem_desc(sbase + kOffP + pb_i * kPBytes, 16, 1024, tc::kSwizzle128);
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+              for (int s = 0; s < 2; ++s)
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+                  tc::mma_f8_ss(tmem + kOCol + 64 * blk,
+                                va + (uint64_t)((blk * kLatBlock + s * 4096) >> 4),
+                                pb + (uint64_t)((64 * part + 32 * s) >> 4),
+                                part ? id_pv_lo : id_pv_hi, !(ps && s == 0 && part == 0));
+            tc::mma_commit(bar(BAR_PAGE_EMPTY + slot));
+            tc::mma_commit(bar(BAR_P_EMPTY + pb_i));
+            tc::mma_commit(bar(BAR_PV_DONE + (int)(k & 1)));
+            if (pe) tc::mma_commit(bar(BAR_O_FULL));
           }
-        }
-        action = __shfl_sync(0xffffffffu, action, 0);
-        if (action < 0) {
-          ok = false;
-          break;
-        }
-        if (action == 1) {
-          pv_issue(pv_next);
-          ++pv_next;
-        } else if (action == 2) {
-          qk_issue(qk_next, desc[qk_next % kDescRing]);
-          ++qk_next;
+          __syncwarp();
         }
       }
       if (leader) {
         if (!ok) abort_cta();
-        // drain: every issued MMA has finished before TMEM is freed
-        tc::mma_commit(bar(BAR_DRAIN));
-        if (!tc::mbar_wait(bar(BAR_DRAIN), 0, kWaitNs)) atomicOr(p.ws.status, MLA_DEVICE_ERR_TIMEOUT);
+        // drain: every MMA this thread issued has finished before TMEM is freed
+        const int db = BAR_DRAIN + (warp == kPvWarp ? 1 : 0);
+        tc::mma_commit(bar(db));
+        if (!tc::mbar_wait(bar(db), 0, kWaitNs)) atomicOr(p.ws.status, MLA_DEVICE_ERR_TIMEOUT);
       }
       __syncwarp();
     } else {
@@ -633,6 +624,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
           grow = true;
         }
+        // P buffer j % 3 was read by PV(j - 3); waiting for it also makes the
+        // PV_DONE parity below unambiguous (PV(j - 3) is complete)
+        if (j >= kPBufs) {
+          const bool got = tc::mbar_wait(bar(BAR_P_EMPTY + (int)(j % kPBufs)),
+                                         (uint32_t)(j / kPBufs - 1) & 1, kWaitNs);
+          if (!got) {
+            flags[F_ABORT] = 1;
+            atomicOr(p.ws.status, MLA_DEVICE_ERR_TIMEOUT);
+          }
+        }
         float* alpha_w = alpha_s + 64 * (int)(j & 1);
         if (part == 0) alpha_w[h] = alpha;
         if (named_bar_softmax_or(grow)) {
@@ -756,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kQkWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
