@@ -14,6 +14,7 @@
 // ulp toward it before the hardware rounds to e4m3. Away from midpoints the
 // float32 rounding cannot change the e4m3 result.
 #include "mla_common.cuh"
+#include "mla_internal.h"
 
 namespace mla {
 namespace {

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/mla.h"
 
 namespace mla {
@@ -16,7 +18,7 @@ struct DecodeWorkspace {
   int32_t* row_np;
   int32_t* piece_err;
   float* part_lse;
-  float* part_out;
+  __nv_bfloat16* part_out;
   uint8_t* q_prep;   // FP8 kernel: prepared q, q_copies copies
   float* q_mul;
   int q_copies;
