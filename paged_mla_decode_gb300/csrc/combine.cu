@@ -84,7 +84,7 @@ constexpr int kInFlight = 8;  // pieces per warp with loads in flight
 __global__ void __launch_bounds__(kPieceThreads)
 combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __restrict__ row_np,
                       const int32_t* __restrict__ piece_err, const float* __restrict__ part_lse,
-                      const __nv_bfloat16* __restrict__ part_out, int heads,
+                      const float* __restrict__ part_out, int heads,
                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   __shared__ float4 s_acc[kPieceWarps][32];
   __shared__ float s_red[kPieceWarps];
@@ -131,10 +131,7 @@ combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __res
           const int64_t piece = (int64_t)(base + s) * heads + h;
           const float l = part_lse[piece];
           wgt[u] = (l > -INFINITY) ? fast_exp2((l - m) * kLog2e) : 0.f;
-          const uint2 raw = *reinterpret_cast<const uint2*>(part_out + piece * kDLatent + dim0);
-          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-          v[u] = make_float4(a.x, a.y, b.x, b.y);
+          v[u] = *reinterpret_cast<const float4*>(part_out + piece * kDLatent + dim0);
         }
       }
 #pragma unroll

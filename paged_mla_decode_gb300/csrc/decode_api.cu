@@ -81,7 +81,7 @@ extern "C" mla_status mla_decode(const void* q, const void* kv_pages, int64_t nu
   p.ws.row_np = reinterpret_cast<int32_t*>(ws + L.row_np);
   p.ws.piece_err = reinterpret_cast<int32_t*>(ws + L.piece_err);
   p.ws.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
-  p.ws.part_out = reinterpret_cast<__nv_bfloat16*>(ws + L.part_out);
+  p.ws.part_out = reinterpret_cast<float*>(ws + L.part_out);
   p.ws.q_prep = ws + L.q_prep;
   p.ws.q_mul = reinterpret_cast<float*>(ws + L.q_mul);
   p.ws.q_copies = L.q_copies;

@@ -726,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           named_bar_softmax();
           if (t == 0) p.ws.piece_err[slot] = bad;
-          __nv_bfloat16* out = p.ws.part_out + (int64_t)slot * H * kDLatent + t;
+          float* out = p.ws.part_out + (int64_t)slot * H * kDLatent + t;
           const int nhalf = (H + 31) >> 5;
 #pragma unroll 1
           for (int blk = 0; blk < 4; ++blk) {
@@ -735,12 +735,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t r[32];
               tc::tmem_ld32(tmem + lane_base + kOCol + 64 * blk + 32 * half, r);
               tc::tmem_wait_ld();
-              __nv_bfloat16* o = out + (int64_t)(32 * half) * kDLatent + 128 * blk;
+              float* o = out + (int64_t)(32 * half) * kDLatent + 128 * blk;
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 if (32 * half + i < H)
                   o[(int64_t)i * kDLatent] =
-                      __float2bfloat16_rn(__uint_as_float(r[i]) * linv_s[32 * half + i]);
+                      (__uint_as_float(r[i]) * linv_s[32 * half + i]);
               }
             }
           }

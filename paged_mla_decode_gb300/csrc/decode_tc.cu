@@ -821,7 +821,7 @@ __global__ void __maxnreg__(168)
           }
           tc::fence_after_sync();
           const int slot = tw.cur.base + (c - plan.cta_of(tw.cur.rt));
-          __nv_bfloat16* out = p.ws.part_out + (int64_t)slot * H * kDLatent + t;
+          float* out = p.ws.part_out + (int64_t)slot * H * kDLatent + t;
           if (t < 64) {
             const float* rs = red_sum + (k & 1) * 256;
             const float l = l_sum[t] + rs[t] + rs[64 + t] + rs[128 + t] + rs[192 + t];
@@ -837,12 +837,12 @@ __global__ void __maxnreg__(168)
               uint32_t r[32];
               tc::tmem_ld32(tmem + lane_base + kOCol + 64 * mt + 32 * half, r);
               tc::tmem_wait_ld();
-              __nv_bfloat16* o = out + (int64_t)(32 * half) * kDLatent + 128 * mt;
+              float* o = out + (int64_t)(32 * half) * kDLatent + 128 * mt;
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 if (32 * half + i < H)
                   o[(int64_t)i * kDLatent] =
-                      __float2bfloat16_rn(__uint_as_float(r[i]) * alpha[32 * half + i]);
+                      (__uint_as_float(r[i]) * alpha[32 * half + i]);
               }
             }
           }

@@ -30,7 +30,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 //   row_np    int32[R]       number of partial slots of the row; -1 = bad length
 //   piece_err int32[P]       1 if the piece met a bad page id
 //   part_lse  float[P][H]    log-sum-exp of each piece (natural log)
-//   part_out  bf16[P][H][512] normalised partial output of each piece
+//   part_out  float[P][H][512] normalised partial output of each piece
 //   q_prep    uint8[C][R][128][576] q of each row as the FP8 kernel's A operand
 //             (row t = head 16*(t/32) + t%16, term (t/16)%2: e4m3 hi / lo),
 //             C copies so that the CTAs sharing a row spread their reads
@@ -64,7 +64,7 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int64_t rows, int he
   w.row_np = off; off = align_up(off + 4 * rows, 256);
   w.piece_err = off; off = align_up(off + 4 * w.max_pieces, 256);
   w.part_lse = off; off = align_up(off + 4 * w.max_pieces * heads, 256);
-  w.part_out = off; off = align_up(off + 2 * w.max_pieces * heads * (int64_t)kDLatent, 256);
+  w.part_out = off; off = align_up(off + 4 * w.max_pieces * heads * (int64_t)kDLatent, 256);
   w.q_copies = q_prep_copies(rows, num_ctas);
   w.q_prep = off; off = align_up(off + (size_t)w.q_copies * rows * kQPrepRowBytes, 256);
   w.q_mul = off; off = align_up(off + 4 * rows * 64, 256);

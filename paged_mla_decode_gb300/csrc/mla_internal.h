@@ -18,7 +18,7 @@ struct DecodeWorkspace {
   int32_t* row_np;
   int32_t* piece_err;
   float* part_lse;
-  __nv_bfloat16* part_out;
+  float* part_out;
   uint8_t* q_prep;   // FP8 kernel: prepared q, q_copies copies
   float* q_mul;
   int q_copies;

@@ -73,6 +73,6 @@ def test_workspace_size_grows_with_ctas(lib):
     a = lib.mla_decode_workspace_size(1, 1, 64, 100)
     b = lib.mla_decode_workspace_size(1, 1, 64, 200)
     assert 0 < a < b
-    # per piece: 64 heads x (512 bf16 outputs + 1 float lse)
-    assert b - a >= 100 * 64 * (512 * 2 + 4)
+    # per piece: 64 heads x (512 + 1) floats
+    assert b - a >= 100 * 64 * 513 * 4
     assert lib.mla_decode_workspace_size(1, 9, 64, 100) == 0
