@@ -423,8 +423,8 @@ def run_gpu(args):
             "steps_per_s": world * steps_per_s, "tokens_per_s": tokens_per_s,
             "kv_gbs": kv_gbs, "pct_of_hbm_peak": 100.0 * kv_gbs / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            # per step: KV append, then q prep (e4m3 caches), decode and combine
-            "gpu_launches": (4 if kv_dtype == "e4m3" else 3) * args.steps, "clocks": clocks,
+            # per step: KV append, decode and combine
+            "gpu_launches": 3 * args.steps, "clocks": clocks,
             "device_status": status,
         }
         print(json.dumps(line), flush=True)

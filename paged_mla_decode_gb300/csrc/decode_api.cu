@@ -82,20 +82,11 @@ extern "C" mla_status mla_decode(const void* q, const void* kv_pages, int64_t nu
   p.ws.piece_err = reinterpret_cast<int32_t*>(ws + L.piece_err);
   p.ws.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   p.ws.part_out = reinterpret_cast<float*>(ws + L.part_out);
-  p.ws.q_prep = ws + L.q_prep;
-  p.ws.q_mul = reinterpret_cast<float*>(ws + L.q_mul);
-  p.ws.q_copies = L.q_copies;
 
   if (!p.bf16 && num_pages > (int64_t)(0x7fffffff / kPageSize)) return MLA_ERR_UNSUPPORTED;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaSuccess;
-  if (p.bf16) {
-    e = launch_decode_tensor_core(p, s);
-  } else {
-    e = launch_q_prep(p.q, (int)rows, num_heads, p.score_mul, p.ws, s);
-    if (e == cudaSuccess) e = launch_decode_fp8(p, s);
-  }
+  cudaError_t e = p.bf16 ? launch_decode_tensor_core(p, s) : launch_decode_fp8(p, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   e = launch_combine_pieces(p.ws, (int)rows, num_heads, G, static_cast<__nv_bfloat16*>(out), lse,
                             s);

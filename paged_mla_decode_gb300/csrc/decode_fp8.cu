@@ -10,8 +10,9 @@
 //   S [128 x 64 tokens]  = A . page^T       A = [q_hi ; q_lo] per head, e4m3
 //   O^T[512 x 64 heads] += V^T . (P_hi + P_lo)^T      V = the page's first 512 dims
 //
-// q (bf16) is scaled per head by a power of two and split into two e4m3 terms
-// q_hi + q_lo, which is exact for bf16 inputs (8 significant bits = 4 + 4), so
+// q (bf16) is scaled per head by a power of two (max |q| in [2^7, 2^8)) and split
+// into two e4m3 terms q_hi = e4m3(q), q_lo = e4m3(q - q_hi), which is exact for
+// bf16 inputs (8 significant bits = 4 + 4) down to 2^-10 of the head's max, so
 // S_hi + S_lo is q . k up to fp32 accumulation. P = 2^(s - m + 6) is split into
 // an e4m3 term and an e5m2 remainder (7 significant bits; the e5m2 range keeps
 // tokens down to 2^-24 of the running maximum). All heads attend over the one latent
@@ -172,74 +173,6 @@ __device__ __forceinline__ uint32_t e5m2x2_of(float lo, float hi) {
   return r;
 }
 
-// q of row blockIdx.x split into the FP8 kernel's A operand, written to copy
-// blockIdx.y. A row t is head 16*(t/32) + t%16, e4m3 term (t/16)%2 (hi, lo); its
-// byte 4i+k is dim 4i+k. The head is scaled by a power of two so that its max |q|
-// lies in [2^7, 2^8), then q_hi = e4m3(q), q_lo = e4m3(q - q_hi): exact for
-// bf16 q (8 significant bits = 4 + 4) down to 2^-10 of the head's max.
-// Four threads per head, 144 dims each.
-__global__ void __launch_bounds__(256)
-    q_prep_kernel(const __nv_bfloat16* __restrict__ q, int rows, int H, float score_mul,
-                  uint8_t* __restrict__ q_prep, float* __restrict__ q_mul) {
-  const int row = blockIdx.x, cp = blockIdx.y;
-  const int h = threadIdx.x >> 2, k4 = threadIdx.x & 3;
-  const bool live = h < H;
-  const uint4* src = reinterpret_cast<const uint4*>(
-      q + ((int64_t)row * H + (live ? h : 0)) * kDEntry + 144 * k4);
-  uint4 w[18];
-#pragma unroll
-  for (int u = 0; u < 18; ++u) w[u] = live ? __ldg(src + u) : make_uint4(0, 0, 0, 0);
-  float amax = 0.f;
-#pragma unroll
-  for (int u = 0; u < 18; ++u) {
-    const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
-      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-    }
-  }
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-  int shift = 0;
-  if (amax > 0.f && isfinite(amax)) {
-    int e;
-    frexpf(amax, &e);
-    shift = 8 - e;  // scaled max in [2^7, 2^8)
-  }
-  const float sc = live ? ldexpf(1.0f, shift) : 0.f;
-  if (k4 == 0 && cp == 0)
-    q_mul[(int64_t)row * 64 + h] = live ? score_mul * ldexpf(1.0f, -shift) : 0.f;
-  const int t_hi = 32 * (h >> 4) + (h & 15);   // A rows of this head's two terms
-  uint8_t* base = q_prep + ((int64_t)cp * rows + row) * kQPrepRowBytes + 144 * k4;
-  uint4* dst_hi = reinterpret_cast<uint4*>(base + (int64_t)t_hi * kDEntry);
-  uint4* dst_lo = reinterpret_cast<uint4*>(base + (int64_t)(t_hi + 16) * kDEntry);
-#pragma unroll
-  for (int u2 = 0; u2 < 9; ++u2) {  // 16 dims -> one 16-byte vector of each term
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const uint4 wv = w[2 * u2 + half];
-      const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-      uint32_t hc[4], lc[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
-        const float x0 = f.x * sc, x1 = f.y * sc;
-        hc[k] = e4m3x2_of(x0, x1);
-        const float2 hv = e4m3x2_value(hc[k]);
-        lc[k] = e4m3x2_of(x0 - hv.x, x1 - hv.y);
-      }
-      hw[2 * half] = hc[0] | (hc[1] << 16);
-      hw[2 * half + 1] = hc[2] | (hc[3] << 16);
-      lw[2 * half] = lc[0] | (lc[1] << 16);
-      lw[2 * half + 1] = lc[2] | (lc[3] << 16);
-    }
-    dst_hi[u2] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    dst_lo[u2] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  }
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fp8_kernel(const Fp8Params p, const __grid_constant__ CUtensorMap lat_map,
                       const __grid_constant__ CUtensorMap rope_map) {
@@ -351,10 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            if (d.flags & kDescPieceStart)  // the softmax warps read this row's q soon
-              tc::prefetch_l2_bulk(
-                  p.ws.q_prep + ((int64_t)(c % p.ws.q_copies) * p.rows + d.row) * kQPrepRowBytes,
-                  (uint32_t)kQPrepRowBytes);
+            if ((d.flags & kDescPieceStart) && j > 0)  // the softmax warps read this q soon
+              tc::prefetch_l2_bulk(p.q + (int64_t)d.row * H * kDEntry,
+                                   (uint32_t)(H * kDEntry * sizeof(__nv_bfloat16)));
             if (d.flags & kDescPageOk) {
               tc::mbar_arrive_expect_tx(bar(BAR_PAGE_FULL + slot), (uint32_t)kPageBytes);
               const int y = d.page * kPageSize;
@@ -534,31 +466,113 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
           }
-          // the prepared row of this thread's lane (copy chosen by CTA index)
-          const uint4* src = reinterpret_cast<const uint4*>(
-              p.ws.q_prep + (((int64_t)(c % p.ws.q_copies) * p.rows + row) * 128 + t) * kDEntry);
-          uint4 w[36];
+          // This thread reads half of its head's 576 dims (part 0: 0-287, part 1:
+          // 288-575) in one batch; the head's max |q| comes from the partner lane.
+          const bool live = h < H;
+          const uint4* qh = reinterpret_cast<const uint4*>(
+                                p.q + ((int64_t)row * H + (live ? h : 0)) * kDEntry) +
+                            36 * part;
+          // max pass over all 36 vectors; round 0's 12 stay in registers, rounds 1
+          // and 2 are read again (from L2) while the previous round converts
+          uint4 w[2][12];
+          float amax = 0.f;
+          {
+            uint4 a[36];
 #pragma unroll
-          for (int u = 0; u < 36; ++u) w[u] = __ldg(src + u);
-          qmul = h < H ? __ldg(p.ws.q_mul + (int64_t)row * 64 + h) : 0.f;
+            for (int u = 0; u < 36; ++u) a[u] = live ? __ldg(qh + u) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
-            uint32_t r[32];
+            for (int u = 0; u < 36; ++u) {
+              const uint32_t ws[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              r[4 * u] = w[8 * blk + u].x;
-              r[4 * u + 1] = w[8 * blk + u].y;
-              r[4 * u + 2] = w[8 * blk + u].z;
-              r[4 * u + 3] = w[8 * blk + u].w;
+              for (int k = 0; k < 4; ++k) {
+                const float2 f =
+                    __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+              }
             }
-            tc::tmem_st32(tmem + lane_base + kQCol + 32 * blk, r);
-          }
-          // rope words: shared memory row t (64 B, 64-byte swizzle)
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint32_t a = sbase + kOffQRope + t * 64 + ((u ^ ((t >> 1) & 3)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(w[32 + u].x),
-                         "r"(w[32 + u].y), "r"(w[32 + u].z), "r"(w[32 + u].w));
+            for (int u = 0; u < 12; ++u) w[0][u] = a[u];
+          }
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
+          int shift = 0;
+          if (amax > 0.f && isfinite(amax)) {
+            int e;
+            frexpf(amax, &e);
+            shift = 8 - e;  // scaled max in [2^7, 2^8)
+          }
+          const float sc = live ? ldexpf(1.0f, shift) : 0.f;
+          qmul = live ? p.score_mul * ldexpf(1.0f, -shift) : 0.f;
+          // Three rounds of 96 dims per thread through the (free) P buffers: each
+          // thread writes the hi codes of its dims to its head's hi row and the lo
+          // codes to the lo row ([128 rows][own 96 B | partner 96 B]), then copies
+          // its own row's 48 words into place: words [24r, 24r+24) and [72+24r, ...)
+          // (word i = codes of dims 4i..4i+3; words 128-143 are the rope).
+          uint8_t* stage = smem + kOffP;
+          const int t_hi = 32 * warp + (lane & 15);
+#pragma unroll
+          for (int r = 0; r < 3; ++r) {
+            if (r < 2) {
+#pragma unroll
+              for (int u = 0; u < 12; ++u)
+                w[(r + 1) & 1][u] = live ? __ldg(qh + 12 * (r + 1) + u) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u2 = 0; u2 < 6; ++u2) {  // 16 dims -> one 16-byte vector of each term
+              uint32_t hw[4], lw[4];
+#pragma unroll
+              for (int half = 0; half < 2; ++half) {
+                const uint4 wv = w[r & 1][2 * u2 + half];
+                const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+                uint32_t hc[4], lc[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float2 f =
+                      __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+                  const float x0 = f.x * sc, x1 = f.y * sc;
+                  hc[k] = e4m3x2_of(x0, x1);
+                  const float2 hv = e4m3x2_value(hc[k]);
+                  lc[k] = e4m3x2_of(x0 - hv.x, x1 - hv.y);
+                }
+                hw[2 * half] = hc[0] | (hc[1] << 16);
+                hw[2 * half + 1] = hc[2] | (hc[3] << 16);
+                lw[2 * half] = lc[0] | (lc[1] << 16);
+                lw[2 * half + 1] = lc[2] | (lc[3] << 16);
+              }
+              const int off = 96 * part + 16 * u2;
+              *reinterpret_cast<uint4*>(stage + t_hi * 192 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint4*>(stage + (t_hi + 16) * 192 + off) =
+                  make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            named_bar_softmax();  // the round's rows are complete
+            const uint32_t* mine = reinterpret_cast<const uint32_t*>(stage + t * 192);
+#pragma unroll
+            for (int g = 0; g < 3; ++g) {  // own dims [96r, 96r+96): TMEM words 24r + 8g
+              uint32_t v8[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v8[i] = mine[8 * g + i];
+              tc::tmem_st8(tmem + lane_base + kQCol + 24 * r + 8 * g, v8);
+            }
+#pragma unroll
+            for (int g = 0; g < 3; ++g) {  // dims [288+96r, ...): words 72 + 24r + 8g
+              uint32_t v8[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v8[i] = mine[24 + 8 * g + i];
+              const int word = 72 + 24 * r + 8 * g;
+              if (word < 128) {
+                tc::tmem_st8(tmem + lane_base + kQCol + word, v8);
+              } else {  // rope: shared memory row t (64 B, 64-byte swizzle)
+                const int u0 = (word - 128) / 4;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                  const uint32_t a =
+                      sbase + kOffQRope + t * 64 + (((u0 + h2) ^ ((t >> 1) & 3)) << 4);
+                  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a),
+                               "r"(v8[4 * h2]), "r"(v8[4 * h2 + 1]), "r"(v8[4 * h2 + 2]),
+                               "r"(v8[4 * h2 + 3]));
+                }
+              }
+            }
+            named_bar_softmax();  // the staging rows are free again
           }
           tc::tmem_wait_st();
           tc::fence_proxy_async_smem();
@@ -762,14 +776,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
-
-cudaError_t launch_q_prep(const __nv_bfloat16* q, int rows, int heads, float score_mul,
-                          const DecodeWorkspace& ws, cudaStream_t stream) {
-  if (rows <= 0) return cudaSuccess;
-  q_prep_kernel<<<dim3((unsigned)rows, (unsigned)ws.q_copies), 256, 0, stream>>>(
-      q, rows, heads, score_mul, ws.q_prep, ws.q_mul);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
   static std::atomic<int> configured[64];

@@ -31,28 +31,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 //   piece_err int32[P]       1 if the piece met a bad page id
 //   part_lse  float[P][H]    log-sum-exp of each piece (natural log)
 //   part_out  float[P][H][512] normalised partial output of each piece
-//   q_prep    uint8[C][R][128][576] q of each row as the FP8 kernel's A operand
-//             (row t = head 16*(t/32) + t%16, term (t/16)%2: e4m3 hi / lo),
-//             C copies so that the CTAs sharing a row spread their reads
-//   q_mul     float[R][64] per-head score multiplier of the prepared q
 //
 // with R = batch * num_queries rows and P = num_ctas + R an upper bound on the
 // number of pieces (each CTA range adds at most one piece per row boundary).
 // ---------------------------------------------------------------------------
-constexpr int kQPrepRowBytes = 128 * kDEntry;  // one row's A operand: 73728 bytes
-
 struct WorkspaceLayout {
-  size_t row_base, row_np, piece_err, part_lse, part_out, q_prep, q_mul, total;
+  size_t row_base, row_np, piece_err, part_lse, part_out, total;
   int64_t max_pieces;
-  int q_copies;
 };
-
-// Copies of the prepared q: about one per 8 CTAs reading a row, at most 16.
-__host__ __device__ inline int q_prep_copies(int64_t rows, int num_ctas) {
-  const int64_t per_row = rows > 0 ? num_ctas / rows : num_ctas;
-  const int64_t c = per_row / 8;
-  return (int)(c < 1 ? 1 : (c > 16 ? 16 : c));
-}
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -65,9 +51,6 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int64_t rows, int he
   w.piece_err = off; off = align_up(off + 4 * w.max_pieces, 256);
   w.part_lse = off; off = align_up(off + 4 * w.max_pieces * heads, 256);
   w.part_out = off; off = align_up(off + 4 * w.max_pieces * heads * (int64_t)kDLatent, 256);
-  w.q_copies = q_prep_copies(rows, num_ctas);
-  w.q_prep = off; off = align_up(off + (size_t)w.q_copies * rows * kQPrepRowBytes, 256);
-  w.q_mul = off; off = align_up(off + 4 * rows * 64, 256);
   w.total = off;
   return w;
 }

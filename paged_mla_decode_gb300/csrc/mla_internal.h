@@ -19,9 +19,6 @@ struct DecodeWorkspace {
   int32_t* piece_err;
   float* part_lse;
   float* part_out;
-  uint8_t* q_prep;   // FP8 kernel: prepared q, q_copies copies
-  float* q_mul;
-  int q_copies;
 };
 
 // Everything a decode kernel launch needs (validated by the caller).
@@ -42,11 +39,6 @@ struct DecodeLaunch {
 
 // Split-KV decode on the tcgen05 tensor cores (decode_tc.cu); heads <= 64.
 cudaError_t launch_decode_tensor_core(const DecodeLaunch& d, cudaStream_t stream);
-
-// q of every row split into the FP8 kernel's A operand (e4m3 hi/lo per head,
-// power-of-two scaled) and score multipliers, written to the workspace.
-cudaError_t launch_q_prep(const __nv_bfloat16* q, int rows, int heads, float score_mul,
-                          const DecodeWorkspace& ws, cudaStream_t stream);
 
 // Split-KV decode with the e4m3 cache bytes as tensor-core operands
 // (decode_fp8.cu); e4m3 caches only, heads <= 64, num_pages * 64 < 2^31.
