@@ -74,6 +74,16 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def slowest_rank_ms(elapsed_ms, dist=None):
+    """The timed region's length on the slowest rank (max over the process group)."""
+    if dist is None:
+        return float(elapsed_ms)
+    import torch
+    tt = torch.tensor([float(elapsed_ms)], dtype=torch.float64)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
 def aggregate(values_ms, units_per_rank):
     """Whole-job throughput: all ranks' units over the slowest rank's time."""
     t = max(values_ms)
@@ -286,12 +296,14 @@ def run_gpu(args):
     out = torch.empty((B, Q, H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Q, H), dtype=torch.float32, device=dev)
     ws = torch.zeros(binding.mla_decode_workspace_size(B, Q, H), dtype=torch.uint8, device=dev)
+    f16_ops = args.operands == "f16"
 
     def step(r, ev=None):
         binding.mla_kv_append(fresh_lat, fresh_rope, fresh_slots[r], pages, kv_scale)
         if ev is not None:
             ev[0].record()
-        binding.mla_decode(q, pages, tables_d[r], seq_lens, w.sm_scale, kv_scale, out, lse, ws)
+        binding.mla_decode(q, pages, tables_d[r], seq_lens, w.sm_scale, kv_scale, out, lse, ws,
+                           f16_operands=f16_ops)
         if ev is not None:
             ev[1].record()
 
@@ -340,10 +352,7 @@ def run_gpu(args):
     decode_ms = [a.elapsed_time(b) for a, b in evs]
     decode_us = 1e3 * sum(decode_ms) / len(decode_ms)
 
-    if dist:
-        tt = torch.tensor([elapsed_ms], dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = slowest_rank_ms(elapsed_ms, dist)
 
     status = binding.read_device_status(ws)
     steps_per_s = args.steps / (elapsed_ms / 1e3)
@@ -376,7 +385,8 @@ def run_gpu(args):
                              (d_lat, h_lat), (d_rope, h_rope), (d_slots, h_slots[r])):
                     d.copy_(h, non_blocking=True)
                 binding.mla_kv_append(d_lat, d_rope, d_slots, pages, kv_scale)
-                binding.mla_decode(d_q, pages, d_table, d_lens, w.sm_scale, kv_scale, out, lse, ws)
+                binding.mla_decode(d_q, pages, d_table, d_lens, w.sm_scale, kv_scale, out, lse, ws,
+                                   f16_operands=f16_ops)
                 h_out.copy_(out, non_blocking=True)
                 h_lse.copy_(lse, non_blocking=True)
             stream.synchronize()
@@ -415,6 +425,7 @@ def run_gpu(args):
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": kv_dtype, "data": "synthetic",
             "config": {"workload": desc, "batch": B, "queries": Q, "heads": H,
+                       "mma_operands": "bf16" if kv_dtype == "bf16" else args.operands,
                        "seq_lens_total": int(w.seq_lens.sum()), "unique_tokens": w.unique_tokens,
                        "kv_dtype": kv_dtype, "page_size": 64,
                        "l2": f"rotating {copies} cache copies "
@@ -440,6 +451,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=100)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=sorted(CONFIGS), default="long")
+    ap.add_argument("--operands", choices=["fp8", "f16"], default="fp8",
+                    help="tensor-core operands for an e4m3 cache: its bytes (mla_decode) or "
+                         "f16 after widening (mla_decode_f16_operands, the ablation)")
     ap.add_argument("--copies", type=int, default=0, help="cache copies rotated (0 = auto)")
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--no-e2e", action="store_true")

@@ -141,6 +141,12 @@ MLA_API size_t mla_decode_workspace_size(int batch, int num_queries, int num_hea
  * (out, lse) that a second kernel merges by log-sum-exp ("vLLM x AgentX",
  * section "Kimi K3"), so one call fills all SMs even at batch 1.
  *
+ * Arithmetic: for an e4m3 cache the cache bytes themselves are the tensor-core
+ * operands (tcgen05 kind::f8f6f4); q is scaled per head by a power of two and
+ * split into two e4m3 terms (exact for bf16 q), the softmax weights into an
+ * e4m3 and an e5m2 term (7 significant bits); accumulation is fp32. For a bf16
+ * cache both contractions use bf16 operands (kind::f16).
+ *
  * q           device, bf16 [batch][num_queries][num_heads][576]
  * kv_pages    device, the cache; num_pages pages of page_size (= 64) tokens
  * block_table device, int32 [batch][max_pages]; entries past a request's last
@@ -163,6 +169,25 @@ MLA_API mla_status mla_decode(const void* q, const void* kv_pages, int64_t num_p
                       const int32_t* seq_lens, int batch, int num_queries, int num_heads,
                       float sm_scale, float kv_scale, int num_ctas, void* workspace,
                       size_t workspace_bytes, void* out, float* lse, mla_stream_t stream);
+
+/*
+ * mla_decode_f16_operands -- mla_decode with 16-bit tensor-core operands.
+ *
+ * Same arguments, contract and results (within the same tolerance) as
+ * mla_decode. For an e4m3 cache the pages are widened to f16 in shared memory
+ * as they are read (the FP8 cache of "Smaller, faster, safer: running Kimi and
+ * GLM at scale", section "Quantizing the KV cache", converted on load) and both
+ * contractions use kind::f16 with q and the softmax weights in f16; for a bf16
+ * cache it is mla_decode. It exists to measure what reading the FP8 bytes as
+ * operands saves; it has no counterpart on the pages.
+ */
+MLA_API mla_status mla_decode_f16_operands(const void* q, const void* kv_pages, int64_t num_pages,
+                                   int page_size, int kv_dtype, const int32_t* block_table,
+                                   int max_pages, const int32_t* seq_lens, int batch,
+                                   int num_queries, int num_heads, float sm_scale,
+                                   float kv_scale, int num_ctas, void* workspace,
+                                   size_t workspace_bytes, void* out, float* lse,
+                                   mla_stream_t stream);
 
 /*
  * mla_decode_combine -- merge partial attention results by log-sum-exp.

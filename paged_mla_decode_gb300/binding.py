@@ -28,8 +28,8 @@ MLA_DEVICE_ERR_BAD_PAGE = 0x1
 MLA_DEVICE_ERR_BAD_LENGTH = 0x2
 
 EXPORTED = ("mla_abi_version", "mla_status_string", "mla_kv_append",
-            "mla_decode_workspace_size", "mla_decode", "mla_decode_combine",
-            "mla_decode_static_scratch")
+            "mla_decode_workspace_size", "mla_decode", "mla_decode_f16_operands",
+            "mla_decode_combine", "mla_decode_static_scratch")
 
 _lib = None
 
@@ -64,6 +64,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                c.c_int, c.c_void_p, c.c_int, c.c_int, c.c_int, c.c_float,
                                c.c_float, c.c_int, c.c_void_p, c.c_size_t, c.c_void_p,
                                c.c_void_p, c.c_void_p]
+    lib.mla_decode_f16_operands.restype = c.c_int
+    lib.mla_decode_f16_operands.argtypes = lib.mla_decode.argtypes
     lib.mla_decode_combine.restype = c.c_int
     lib.mla_decode_combine.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_void_p,
                                        c.c_void_p, c.c_void_p]
@@ -127,8 +129,11 @@ def mla_decode_workspace_size(batch: int, num_queries: int, num_heads: int,
 def mla_decode(q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tensor,
                seq_lens: torch.Tensor, sm_scale: float, kv_scale: float, out: torch.Tensor,
                lse: torch.Tensor, workspace: torch.Tensor, num_ctas: int = 0,
-               stream=None) -> None:
-    """Split-KV paged MLA decode (combine included) into ``out`` and ``lse``."""
+               stream=None, f16_operands: bool = False) -> None:
+    """Split-KV paged MLA decode (combine included) into ``out`` and ``lse``.
+
+    ``f16_operands`` calls mla_decode_f16_operands (the e4m3 cache widened to f16
+    operands) instead of mla_decode."""
     assert q.dtype == torch.bfloat16 and q.dim() == 4 and q.shape[3] == 576 and q.is_contiguous()
     batch, nq, heads, _ = q.shape
     assert block_table.dtype == torch.int32 and block_table.dim() == 2
@@ -137,13 +142,15 @@ def mla_decode(q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tenso
     assert out.dtype == torch.bfloat16 and tuple(out.shape) == (batch, nq, heads, 512)
     assert lse.dtype == torch.float32 and tuple(lse.shape) == (batch, nq, heads)
     assert kv_pages.is_contiguous() and kv_pages.dim() == 3 and kv_pages.shape[2] == 576
-    st = load_library().mla_decode(
+    lib = load_library()
+    fn = lib.mla_decode_f16_operands if f16_operands else lib.mla_decode
+    st = fn(
         _ptr(q), _ptr(kv_pages), int(kv_pages.shape[0]), int(kv_pages.shape[1]),
         kv_dtype_code(kv_pages), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
         batch, nq, heads, float(sm_scale), float(kv_scale), int(num_ctas), _ptr(workspace),
         int(workspace.numel() * workspace.element_size()), _ptr(out), _ptr(lse),
         _stream(stream))
-    _check(st, "mla_decode")
+    _check(st, "mla_decode_f16_operands" if f16_operands else "mla_decode")
 
 
 def mla_decode_combine(part_out: torch.Tensor, part_lse: torch.Tensor, out: torch.Tensor,

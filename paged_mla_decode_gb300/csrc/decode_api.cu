@@ -34,12 +34,13 @@ extern "C" size_t mla_decode_workspace_size(int batch, int num_queries, int num_
   return mla::workspace_layout((int64_t)batch * num_queries, num_heads, num_ctas).total;
 }
 
-extern "C" mla_status mla_decode(const void* q, const void* kv_pages, int64_t num_pages,
-                                 int page_size, int kv_dtype, const int32_t* block_table,
-                                 int max_pages, const int32_t* seq_lens, int batch,
-                                 int num_queries, int num_heads, float sm_scale, float kv_scale,
-                                 int num_ctas, void* workspace, size_t workspace_bytes, void* out,
-                                 float* lse, mla_stream_t stream) {
+namespace {
+mla_status decode_impl(const void* q, const void* kv_pages, int64_t num_pages, int page_size,
+                       int kv_dtype, const int32_t* block_table, int max_pages,
+                       const int32_t* seq_lens, int batch, int num_queries, int num_heads,
+                       float sm_scale, float kv_scale, int num_ctas, void* workspace,
+                       size_t workspace_bytes, void* out, float* lse, mla_stream_t stream,
+                       bool f16_operands) {
   using namespace mla;
   if (batch < 0 || num_pages < 0 || max_pages < 1 || num_ctas < 0) return MLA_ERR_INVALID_ARG;
   if (num_queries < 1 || num_queries > MLA_MAX_QUERIES) return MLA_ERR_INVALID_ARG;
@@ -86,9 +87,35 @@ extern "C" mla_status mla_decode(const void* q, const void* kv_pages, int64_t nu
   if (!p.bf16 && num_pages > (int64_t)(0x7fffffff / kPageSize)) return MLA_ERR_UNSUPPORTED;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = p.bf16 ? launch_decode_tensor_core(p, s) : launch_decode_fp8(p, s);
+  cudaError_t e = (p.bf16 || f16_operands) ? launch_decode_tensor_core(p, s)
+                                            : launch_decode_fp8(p, s);
   if (e != cudaSuccess) return MLA_ERR_CUDA;
   e = launch_combine_pieces(p.ws, (int)rows, num_heads, G, static_cast<__nv_bfloat16*>(out), lse,
                             s);
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" mla_status mla_decode(const void* q, const void* kv_pages, int64_t num_pages,
+                                 int page_size, int kv_dtype, const int32_t* block_table,
+                                 int max_pages, const int32_t* seq_lens, int batch,
+                                 int num_queries, int num_heads, float sm_scale, float kv_scale,
+                                 int num_ctas, void* workspace, size_t workspace_bytes, void* out,
+                                 float* lse, mla_stream_t stream) {
+  return decode_impl(q, kv_pages, num_pages, page_size, kv_dtype, block_table, max_pages,
+                     seq_lens, batch, num_queries, num_heads, sm_scale, kv_scale, num_ctas,
+                     workspace, workspace_bytes, out, lse, stream, false);
+}
+
+extern "C" mla_status mla_decode_f16_operands(const void* q, const void* kv_pages,
+                                              int64_t num_pages, int page_size, int kv_dtype,
+                                              const int32_t* block_table, int max_pages,
+                                              const int32_t* seq_lens, int batch,
+                                              int num_queries, int num_heads, float sm_scale,
+                                              float kv_scale, int num_ctas, void* workspace,
+                                              size_t workspace_bytes, void* out, float* lse,
+                                              mla_stream_t stream) {
+  return decode_impl(q, kv_pages, num_pages, page_size, kv_dtype, block_table, max_pages,
+                     seq_lens, batch, num_queries, num_heads, sm_scale, kv_scale, num_ctas,
+                     workspace, workspace_bytes, out, lse, stream, true);
 }

@@ -56,7 +56,7 @@ def oracle_fill_cache(w, kv_dtype="e4m3"):
 
 
 def gpu_decode(w, pages, dev, num_ctas=0, q_bits=None, seq_lens=None, block_table=None,
-               kv_scale=None, workspace=None):
+               kv_scale=None, workspace=None, f16_operands=False):
     q = bf16_tensor(w.q_bits if q_bits is None else q_bits, dev)
     table = torch.from_numpy(w.block_table if block_table is None else block_table).to(dev)
     lens = torch.from_numpy(w.seq_lens if seq_lens is None else seq_lens).to(dev)
@@ -68,7 +68,7 @@ def gpu_decode(w, pages, dev, num_ctas=0, q_bits=None, seq_lens=None, block_tabl
                                 dtype=torch.uint8, device=dev)
     scale = w.kv_scale if kv_scale is None else kv_scale
     binding.mla_decode(q, pages, table, lens, w.sm_scale, scale, out, lse, workspace,
-                       num_ctas=num_ctas)
+                       num_ctas=num_ctas, f16_operands=f16_operands)
     torch.cuda.synchronize()
     return out.float().cpu().numpy(), lse.cpu().numpy(), workspace
 

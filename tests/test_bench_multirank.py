@@ -1,0 +1,72 @@
+"""bench.py's multi-process host logic on CPU: two gloo ranks, no GPU.
+
+Each rank of `bench.py --gpus N` runs an independent replica (the decode path has
+no exchange step); rank 0 reports all ranks' work over the slowest rank's time.
+"""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, times, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        assert bench._rank_env() == (rank, world, rank)
+        t = bench.slowest_rank_ms(times[rank], dist)
+        value, tmax = bench.aggregate([t] * world, [1000] * world)
+        out.put((rank, t, value, tmax))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_report_the_slowest_rank():
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    times = [12.5, 20.0]
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, times, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs)
+    got = sorted(out.get(timeout=10) for _ in range(2))
+    for rank, t, value, tmax in got:
+        assert t == 20.0 and tmax == 20.0
+        # 2 ranks x 1000 units over the slowest rank's 20 ms
+        assert value == pytest.approx(2000 / 0.020)
+
+
+def _reference_rank(rank, world, out):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    out.put((rank, bench.main(["--impl", "reference", "--gpus", str(world),
+                               "--steps", "1", "--warmup", "3"])))
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    p = ctx.Process(target=_reference_rank, args=(1, 2, out))
+    p.start()
+    p.join(timeout=60)
+    assert p.exitcode == 0
+    assert out.get(timeout=10) == (1, 0)
