@@ -201,7 +201,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-// e4m3 pair -> f16 pair (exact: every e4m3 value is an f16 normal number).
 // L2 policy for data read once (the KV stream): its lines are the first to be
 // evicted, so that code, q and page tables stay resident in L2.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
@@ -217,6 +216,7 @@ __device__ __forceinline__ uint4 ld_stream_16(const void* p, uint64_t pol) {
                : "l"(p), "l"(pol));
   return v;
 }
+// e4m3 pair -> f16 pair (exact: every e4m3 value is an f16 normal number).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(v));
