@@ -21,11 +21,14 @@
 // serve trillions of tokens ...", section "First, understand the workload").
 //
 // Warp roles (224 threads):
-//   warps 0-3  q staging, softmax and epilogue. Thread t owns TMEM lane t: row t
-//              of A and S is (head 16*(t/32) + t%16, part (t/16)%2), part 0 = hi,
-//              1 = lo, so the two terms of a head meet inside one warp; for O^T
+//   warps 0-3  q staging, softmax and epilogue. Row t of A and S is (head
+//              16*(t/32) + t%16, part (t/16)%2), part 0 = hi, 1 = lo. Thread t
+//              handles head 16*(t/32) + t%16 and tokens 32*((t/16)%2) .. +31 of a
+//              page: it reads both terms' rows of its half-page (a half-split
+//              TMEM load), so no exchange between threads is needed; for O^T
 //              lane t is dim t of each 128-dim block.
-//   warp 4     TMA producer: pages into a ring of kRing shared-memory slots
+//   warp 4     TMA producer (lane 0): page ids from the block table a window of
+//              pages ahead, pages into a ring of kRing shared-memory slots
 //              (128-byte swizzled latent blocks, 64-byte swizzled rope block).
 //   warp 5     TMEM allocation; issues QK (lane 0) after zeroing the rows of a
 //              partial page past its last token.
@@ -75,6 +78,7 @@ constexpr int kOffLinv = kOffAlpha + 512;                   // float [64]
 constexpr int kOffFlags = kOffLinv + 256;                   // int [4]
 constexpr int kOffPlan = kOffFlags + 16;                    // int64 [6]
 constexpr int kDescRing = 64;                               // page descriptors in flight
+constexpr int kTableAhead = 32;  // pages described (block-table read started) before issue
 constexpr int kOffDesc = kOffPlan + 48;                     // PageDesc [kDescRing]
 constexpr int kOffBar = kOffDesc + 16 * kDescRing;
 constexpr int BAR_PAGE_FULL = 0;              // [kRing] TMA bytes (or zero fill) landed
@@ -122,18 +126,30 @@ struct Fp8Params {
   DecodeWorkspace ws;
 };
 
-// Cursor over a CTA's pages (one page per step).
+// Cursor over a CTA's pages (one page per step). The row's partial slot and
+// block-table offset are computed once per row: a step costs no division.
 struct PageWalker {
   Plan plan;
   RowCursor cur;
   int64_t x, x_end, x_begin;
+  int cta;         // this CTA's index
+  int slot;        // partial slot of the current row's piece in this CTA
+  int64_t bt_row;  // block-table offset of the current row's request
 
-  __device__ void init(const Plan& p, const RowCursor& c, int64_t xb, int64_t xe) {
-    plan = p; cur = c; x = xb; x_begin = xb; x_end = xe;
+  __device__ void init(const Plan& p, const RowCursor& c, int cta_index, int64_t xb, int64_t xe) {
+    plan = p; cur = c; cta = cta_index; x = xb; x_begin = xb; x_end = xe;
+    row_changed();
     settle();
   }
+  __device__ void row_changed() {
+    slot = cur.base + (cta - plan.cta_of(cur.rt));
+    bt_row = (int64_t)(cur.r / plan.nq) * plan.max_pages;
+  }
   __device__ void settle() {
-    if (x < x_end && x == cur.rt + cur.t) cursor_next_row(plan, cur);
+    if (x < x_end && x == cur.rt + cur.t) {
+      cursor_next_row(plan, cur);
+      row_changed();
+    }
   }
   __device__ int page_in_row() const { return (int)(x - cur.rt); }
   __device__ bool piece_start() const { return x == x_begin || x == cur.rt; }
@@ -243,68 +259,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   const PageDesc* desc = reinterpret_cast<const PageDesc*>(smem + kOffDesc);
   if (x_begin < x_end) {
     if (warp == kTmaWarp) {
-      // =================== TMA producer ===================
-      // The warp walks the plan 32 pages at a time: lane i takes page j0 + i, so the
-      // 32 block-table reads are in flight together; lane 0 then issues the copies.
-      const uint64_t pol = l2_evict_first_policy();
-      PageDesc* ring = reinterpret_cast<PageDesc*>(smem + kOffDesc);
-      PageWalker pw;
-      pw.init(plan, cur0, x_begin, x_end);
-      int64_t j = 0;
-      bool ok = true;
-      for (int64_t j0 = 0; j0 < npages && ok; j0 += 32) {
-        PageDesc mine{-1, 0, 0, 0, 0};
-        int64_t bt = -1;
-        for (int i = 0; i < 32 && j0 + i < npages; ++i) {
-          if (lane == i) {
-            mine.valid = (int16_t)pw.valid_tokens();
-            mine.flags = (int16_t)((pw.piece_start() ? kDescPieceStart : 0) |
-                                   (pw.piece_end() ? kDescPieceEnd : 0));
-            mine.row = pw.cur.r;
-            mine.slot = pw.cur.base + (c - plan.cta_of(pw.cur.rt));
-            bt = (int64_t)(pw.cur.r / p.nq) * p.max_pages + pw.page_in_row();
-          }
-          pw.next();
-        }
-        if (bt >= 0) {
-          mine.page = __ldg(p.block_table + bt);
-          if (mine.page >= 0 && (int64_t)mine.page < p.num_pages) mine.flags |= kDescPageOk;
-          ring[(j0 + lane) % kDescRing] = mine;
-        }
-        __syncwarp();
-        if (lane == 0) {
-          for (; j < j0 + 32 && j < npages; ++j) {
-            const PageDesc d = ring[j % kDescRing];
-            const int slot = (int)(j % kRing);
-            const uint32_t round = (uint32_t)(j / kRing);
-            const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
-            if (j >= kRing &&
-                (!tc::mbar_wait(bar(BAR_PAGE_EMPTY + slot), (round - 1) & 1, kWaitNs) ||
-                 flags[F_ABORT])) {
-              ok = false;
-              break;
-            }
-            if ((d.flags & kDescPieceStart) && j > 0)  // the softmax warps read this q soon
-              tc::prefetch_l2_bulk(p.q + (int64_t)d.row * H * kDEntry,
-                                   (uint32_t)(H * kDEntry * sizeof(__nv_bfloat16)));
-            if (d.flags & kDescPageOk) {
-              tc::mbar_arrive_expect_tx(bar(BAR_PAGE_FULL + slot), (uint32_t)kPageBytes);
-              const int y = d.page * kPageSize;
-#pragma unroll
-              for (int b = 0; b < 4; ++b)
-                tc::tma_load_2d_hint(page_base + b * kLatBlock, &lat_map, 128 * b, y,
-                                     bar(BAR_PAGE_FULL + slot), pol);
-              tc::tma_load_2d_hint(page_base + kRopeOff, &rope_map, kDLatent, y,
-                                   bar(BAR_PAGE_FULL + slot), pol);
-            } else {
-              tc::mbar_arrive(bar(BAR_PAGE_FULL + slot));  // bad id: the MMA warp zero-fills
-            }
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        j = __shfl_sync(0xffffffffu, j, 0);
-      }
+      // =================== TMA producer (lane 0) ===================
+      // Lane 0 describes each page kTableAhead pages before it issues the page's
+      // copy: the descriptor fields come from the walker and the physical page id
+      // from an asynchronous 4-byte copy of the block-table entry, so a table read
+      // that misses L2 (over 10 us behind a full stream of page copies) never
+      // holds up the copies. The warp's other lanes have nothing to do.
       if (lane == 0) {
+        const uint64_t pol = l2_evict_first_policy();
+        PageDesc* ring = reinterpret_cast<PageDesc*>(smem + kOffDesc);
+        PageWalker pw;
+        pw.init(plan, cur0, c, x_begin, x_end);
+        int64_t jn = 0;  // next page to describe
+        auto describe_next = [&]() {
+          PageDesc& d = ring[jn % kDescRing];
+          const bool ps = pw.piece_start();
+          d.valid = (int16_t)pw.valid_tokens();
+          d.flags = (int16_t)((ps ? kDescPieceStart : 0) | (pw.piece_end() ? kDescPieceEnd : 0));
+          d.row = pw.cur.r;
+          d.slot = pw.slot;
+          cp_async_4(smem_u32(&d.page), p.block_table + pw.bt_row + pw.page_in_row());
+          cp_async_commit();
+          if (ps && jn > 0)  // the softmax warps read this row's q when they reach it
+            tc::prefetch_l2_bulk(p.q + (int64_t)pw.cur.r * H * kDEntry,
+                                 (uint32_t)(H * kDEntry * sizeof(__nv_bfloat16)));
+          pw.next();
+          ++jn;
+        };
+        // the first copies go out as soon as their table entries are in; the
+        // look-ahead window fills up two pages per issued page
+        while (jn < kRing && jn < npages) describe_next();
+        int64_t j = 0;
+        bool ok = true;
+        for (; j < npages; ++j) {
+          // page j's table read is the oldest of the jn - j groups in flight
+          cp_async_wait_upto<kTableAhead>((int)(jn - j - 1));
+          PageDesc* d = ring + j % kDescRing;
+          const int32_t page = d->page;
+          const bool page_ok = page >= 0 && (int64_t)page < p.num_pages;
+          if (page_ok) d->flags |= kDescPageOk;
+          const int slot = (int)(j % kRing);
+          const uint32_t round = (uint32_t)(j / kRing);
+          const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
+          if (j >= kRing &&
+              (!tc::mbar_wait(bar(BAR_PAGE_EMPTY + slot), (round - 1) & 1, kWaitNs) ||
+               flags[F_ABORT])) {
+            ok = false;
+            break;
+          }
+          if (page_ok) {
+            tc::mbar_arrive_expect_tx(bar(BAR_PAGE_FULL + slot), (uint32_t)kPageBytes);
+            const int y = page * kPageSize;
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+              tc::tma_load_2d_hint(page_base + b * kLatBlock, &lat_map, 128 * b, y,
+                                   bar(BAR_PAGE_FULL + slot), pol);
+            tc::tma_load_2d_hint(page_base + kRopeOff, &rope_map, kDLatent, y,
+                                 bar(BAR_PAGE_FULL + slot), pol);
+          } else {
+            tc::mbar_arrive(bar(BAR_PAGE_FULL + slot));  // bad id: the MMA warp zero-fills
+          }
+          for (int u = 0; u < 2 && jn < npages && jn <= j + kTableAhead; ++u) describe_next();
+        }
+        cp_async_wait<0>();
         if (!ok) abort_cta();
         // no copy may land after the CTA exits: wait for the last issued pages
         for (int64_t jj = j > kRing ? j - kRing : 0; jj < j; ++jj)
@@ -581,14 +598,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) tc::mbar_arrive(bar(BAR_Q_READY));
         }
         // ---- S of this page ----
-        {
-          const bool got =
-              tc::mbar_wait(bar(BAR_S_FULL + (int)(j & 1)), (uint32_t)(j >> 1) & 1, kWaitNs);
-          if (named_bar_softmax_or(!got || flags[F_ABORT])) {
-            ok = false;
-            break;
-          }
-        }
+        // (a failed wait, like a stop by another role, is acted on at this page's
+        // group barrier below: one barrier per page)
+        if (!tc::mbar_wait(bar(BAR_S_FULL + (int)(j & 1)), (uint32_t)(j >> 1) & 1, kWaitNs))
+          flags[F_ABORT] = 1;
         // page validity (tokens of a bad page id are masked and reported)
         const PageDesc d = desc[j % kDescRing];
         const bool pe = d.flags & kDescPieceEnd;
@@ -599,31 +612,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicOr(p.ws.status, MLA_DEVICE_ERR_BAD_PAGE);
         }
         tc::fence_after_sync();
-        float v[64];
-        {
-          uint32_t r[32];
-          tc::tmem_ld32(tmem + lane_base + s_col((int)(j & 1)), r);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          tc::tmem_ld32(tmem + lane_base + s_col((int)(j & 1)) + 32, r);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r[i]);
-        }
+        // both terms of this thread's 32 tokens: rows 32w .. 32w+15 hold q_hi . k of
+        // heads 16w .. 16w+15, rows 32w+16 .. 32w+31 q_lo . k; a half-warp reads
+        // one half of the page's 64 columns
+        uint32_t shi[32], slo[32];
+        tc::tmem_ld16x2_32(tmem + ((uint32_t)(32 * warp) << 16) + s_col((int)(j & 1)), shi);
+        tc::tmem_ld16x2_32(tmem + ((uint32_t)(32 * warp + 16) << 16) + s_col((int)(j & 1)), slo);
+        tc::tmem_wait_ld();
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(bar(BAR_S_EMPTY + (int)(j & 1)));
-        // hi + lo of this thread's 32 tokens (the partner lane holds the other term)
         float s[32];
         float tmax = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float send = part ? v[i] : v[32 + i];
-          const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-          const float mine = part ? v[32 + i] : v[i];
           const bool vis = 32 * part + i < nvis;
-          s[i] = vis ? (mine + recv) * qmul : -INFINITY;
+          s[i] = vis ? (__uint_as_float(shi[i]) + __uint_as_float(slo[i])) * qmul : -INFINITY;
           tmax = fmaxf(tmax, s[i]);
         }
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
@@ -640,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P buffer j % 3 was read by PV(j - 3); waiting for it also makes the
         // PV_DONE parity below unambiguous (PV(j - 3) is complete)
-        if (j >= kPBufs) {
+        if (j >= kPBufs && !flags[F_ABORT]) {
           const bool got = tc::mbar_wait(bar(BAR_P_EMPTY + (int)(j % kPBufs)),
                                          (uint32_t)(j / kPBufs - 1) & 1, kWaitNs);
           if (!got) {
@@ -650,8 +654,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float* alpha_w = alpha_s + 64 * (int)(j & 1);
         if (part == 0) alpha_w[h] = alpha;
-        if (named_bar_softmax_or(grow)) {
-          // rare: bring O^T (PV of the previous page done) to the new maxima
+        if (named_bar_softmax_or(grow || flags[F_ABORT] != 0)) {
+          // rare: a stop, or a head's max grew
+          if (named_bar_softmax_or(flags[F_ABORT] != 0)) {
+            ok = false;
+            break;
+          }
+          // bring O^T (PV of the previous page done) to the new maxima
           const bool got =
               tc::mbar_wait(bar(BAR_PV_DONE + (int)((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1,
                             kWaitNs);

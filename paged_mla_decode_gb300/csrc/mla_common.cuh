@@ -195,10 +195,24 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int s
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                "r"(src_bytes));
 }
+// 4-byte async copy global->shared (both addresses 4-byte aligned).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+// Waits until at most n (0..N) of this thread's groups are pending; n > N counts as N.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+  if constexpr (N == 0) {
+    cp_async_wait<0>();
+  } else {
+    if (n >= N) cp_async_wait<N>();
+    else cp_async_wait_upto<N - 1>(n);
+  }
 }
 
 // L2 policy for data read once (the KV stream): its lines are the first to be
