@@ -464,14 +464,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         int row = cur0.r;
         bool ps = j == 0;
         if (j > 0) {
-          const bool got = tc::mbar_wait(bar(BAR_PAGE_FULL + (int)(j % kRing)),
-                                         (uint32_t)(j / kRing) & 1, kWaitNs);
-          if (named_bar_softmax_or(!got || flags[F_ABORT])) {
-            ok = false;
-            break;
-          }
+          // (a failed wait is acted on at this page's group barrier below; every
+          // thread reads the same descriptor word, so the piece-start decision, and
+          // with it the barriers of the q staging, is uniform either way)
+          if (!tc::mbar_wait(bar(BAR_PAGE_FULL + (int)(j % kRing)), (uint32_t)(j / kRing) & 1,
+                             kWaitNs))
+            flags[F_ABORT] = 1;
           const PageDesc d0 = desc[j % kDescRing];
-          row = d0.row;
+          row = min(max(d0.row, 0), p.rows - 1);  // in range even if a stopped producer never wrote it
           ps = d0.flags & kDescPieceStart;
         }
         if (ps) {
