@@ -17,7 +17,8 @@ Sources (web pages the method is described on):
 * [CF] "Smaller, faster, safer: running Kimi and GLM at scale" (Cloudflare).
   Section "Quantizing the KV cache": the cache is stored as FP8 e4m3 and the
   attention kernel converts values as it reads them. Section "Protecting a
-  shared KV cache": many requests read pages of one physical paged cache.
+  shared KV cache": many requests read pages of one physical paged cache, and
+  a per-page tag that changes on reallocation is checked before decode reads.
 * [vLLM] "vLLM x AgentX: Optimizing for Real-World Agentic Serving".
   Section "Kimi K3": MLA keeps one latent head; decode context parallelism
   produces partial attention outputs plus log-sum-exp statistics that are
@@ -30,9 +31,12 @@ Modules:
 * :mod:`oracle.attention` -- page gather, dequantisation, causal draft
   visibility, float64 softmax attention, log-sum-exp merge, and a brute-force
   dense path for tiny inputs.
+* :mod:`oracle.integrity` -- the KV-cache integrity check of [CF] section
+  "Protecting a shared KV cache": per-request comparison of the pages' current
+  tags with the tags the request expects, one status word per request.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 library routines, brute force and invariants (see each test's docstring).
 """
 
-from . import attention, e4m3  # noqa: F401
+from . import attention, e4m3, integrity  # noqa: F401
