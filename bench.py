@@ -401,6 +401,39 @@ def run_gpu(args):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
                "ms_per_step": e2e_dt * 1e3}
 
+    # ---- the integrity check ("Protecting a shared KV cache"): a separate pass
+    # before decode; its time per call beside the decode call's ----
+    kv_check = None
+    if not args.no_check:
+        rng = np.random.default_rng(5)
+        tags = torch.from_numpy(rng.integers(-2**31, 2**31, size=pages.shape[0],
+                                             dtype=np.int64).astype(np.int32)).to(dev)
+        expected = tags[tables_d[0].clamp(min=0).long()].contiguous()
+        chk_status = torch.full((B,), -1, dtype=torch.int32, device=dev)
+        chk_lens = torch.empty_like(seq_lens)
+        per_graph = 20
+        with torch.cuda.stream(stream):
+            binding.mla_kv_check(tags, tables_d[0], expected, seq_lens, chk_status, chk_lens)
+        torch.cuda.synchronize()
+        gck = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gck, stream=stream):
+            for _ in range(per_graph):
+                binding.mla_kv_check(tags, tables_d[0], expected, seq_lens, chk_status, chk_lens)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                gck.replay()
+            c0.record()
+            reps = 20
+            for _ in range(reps):
+                gck.replay()
+            c1.record()
+        torch.cuda.synchronize()
+        check_us = 1e3 * c0.elapsed_time(c1) / (reps * per_graph)
+        kv_check = {"us_per_call": check_us, "fraction_of_decode_call": check_us / decode_us,
+                    "requests_failed": int((chk_status != 0).sum().item()),
+                    "pages_checked": int(sum(-(-int(n) // 64) for n in w.seq_lens))}
+
     peak, peak_kind = measured_peaks()
     decode_bytes = sb["total"]
     achieved = decode_bytes / (decode_us * 1e-6) / 1e9
@@ -433,7 +466,7 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}"},
             "steps_per_s": world * steps_per_s, "tokens_per_s": tokens_per_s,
             "kv_gbs": kv_gbs, "pct_of_hbm_peak": 100.0 * kv_gbs / peak,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "kv_check": kv_check,
             # per step: KV append, decode and combine
             "gpu_launches": 3 * args.steps, "clocks": clocks,
             "device_status": status,
@@ -458,6 +491,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-check", action="store_true",
+                    help="skip timing the integrity check (mla_kv_check) beside the decode")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -209,6 +209,49 @@ MLA_API mla_status mla_decode_combine(const float* part_out, const float* part_l
                               int64_t num_rows, void* out, float* lse, mla_stream_t stream);
 
 /*
+ * mla_kv_check -- integrity check of requests' page mappings before decode.
+ *
+ * The check of "Smaller, faster, safer: running Kimi and GLM at scale",
+ * section "Protecting a shared KV cache": every physical page carries a tag
+ * that the page allocator changes whenever it hands the page out again; each
+ * request keeps, beside its block-table entries, the tags its pages had when it
+ * was given them; before decode reads the cache the two are compared, and a
+ * request with any mismatch is aborted instead of reading another request's
+ * data. It is a separate batch pass, not part of the attention kernel.
+ *
+ * For request b < batch with L = seq_lens[b], over its used logical pages
+ * j < ceil(L / page_size), with p = block_table[b][j]:
+ *   MLA_KV_CHECK_PAGE_RANGE   if p < 0 or p >= num_pages;
+ *   MLA_KV_CHECK_TAG_MISMATCH if page_tags[p] != expected_tags[b][j];
+ *   MLA_KV_CHECK_BAD_LENGTH   (and no page looked at) if L < 0 or
+ *                             L > max_pages * page_size.
+ * request_status[b] = OR of the bits (0 = the request passed);
+ * checked_seq_lens[b] = L if it passed, else -1. Passing checked_seq_lens to
+ * mla_decode as seq_lens aborts the failed requests there: each of their rows
+ * gets out = 0 and lse = -inf (and MLA_DEVICE_ERR_BAD_LENGTH in the workspace
+ * status word) and none of their pages is read.
+ *
+ * page_tags        device, uint32 [num_pages] (may be NULL if num_pages == 0)
+ * block_table      device, int32 [batch][max_pages]; entries past a request's
+ *                  used pages are not read
+ * expected_tags    device, uint32 [batch][max_pages], beside block_table
+ * seq_lens         device, int32 [batch]
+ * page_size        must be 64
+ * request_status   device, uint32 [batch] (written)
+ * checked_seq_lens device, int32 [batch] (written; may be the same buffer as
+ *                  seq_lens only if no other work reads seq_lens concurrently)
+ * Pointers need 4-byte alignment here. Tags are opaque 32-bit values.
+ */
+#define MLA_KV_CHECK_TAG_MISMATCH 0x1u
+#define MLA_KV_CHECK_PAGE_RANGE 0x2u
+#define MLA_KV_CHECK_BAD_LENGTH 0x4u
+MLA_API mla_status mla_kv_check(const uint32_t* page_tags, int64_t num_pages,
+                                const int32_t* block_table, const uint32_t* expected_tags,
+                                int max_pages, const int32_t* seq_lens, int batch, int page_size,
+                                uint32_t* request_status, int32_t* checked_seq_lens,
+                                mla_stream_t stream);
+
+/*
  * mla_decode_static_scratch -- mla_decode for callers that cannot allocate.
  *
  * No counterpart on the pages: this entry point exists for callers that may not

@@ -27,9 +27,13 @@ MLA_KV_BF16 = 1
 MLA_DEVICE_ERR_BAD_PAGE = 0x1
 MLA_DEVICE_ERR_BAD_LENGTH = 0x2
 
+MLA_KV_CHECK_TAG_MISMATCH = 0x1
+MLA_KV_CHECK_PAGE_RANGE = 0x2
+MLA_KV_CHECK_BAD_LENGTH = 0x4
+
 EXPORTED = ("mla_abi_version", "mla_status_string", "mla_kv_append",
             "mla_decode_workspace_size", "mla_decode", "mla_decode_f16_operands",
-            "mla_decode_combine", "mla_decode_static_scratch")
+            "mla_decode_combine", "mla_kv_check", "mla_decode_static_scratch")
 
 _lib = None
 
@@ -69,6 +73,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_decode_combine.restype = c.c_int
     lib.mla_decode_combine.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_void_p,
                                        c.c_void_p, c.c_void_p]
+    lib.mla_kv_check.restype = c.c_int
+    lib.mla_kv_check.argtypes = [c.c_void_p, c.c_int64, c.c_void_p, c.c_void_p, c.c_int,
+                                 c.c_void_p, c.c_int, c.c_int, c.c_void_p, c.c_void_p,
+                                 c.c_void_p]
     lib.mla_decode_static_scratch.restype = c.c_int
     lib.mla_decode_static_scratch.argtypes = [
         c.c_void_p, c.c_void_p, c.c_int64, c.c_int, c.c_int, c.c_void_p, c.c_int, c.c_void_p,
@@ -165,6 +173,35 @@ def mla_decode_combine(part_out: torch.Tensor, part_lse: torch.Tensor, out: torc
     st = load_library().mla_decode_combine(_ptr(part_out), _ptr(part_lse), num_parts, rows,
                                            _ptr(out), _ptr(lse), _stream(stream))
     _check(st, "mla_decode_combine")
+
+
+def mla_kv_check(page_tags: torch.Tensor, block_table: torch.Tensor,
+                 expected_tags: torch.Tensor, seq_lens: torch.Tensor,
+                 request_status: torch.Tensor, checked_seq_lens: torch.Tensor,
+                 stream=None) -> None:
+    """Compare each request's expected page tags with the pages' current tags.
+
+    ``page_tags [num_pages]`` and ``expected_tags [batch, max_pages]`` hold 32-bit
+    tags (int32 or uint32 tensors; compared as unsigned), ``block_table`` and
+    ``seq_lens`` are the decode call's. Writes ``request_status [batch]``
+    (MLA_KV_CHECK_* bits, int32) and ``checked_seq_lens [batch]`` (the lengths,
+    -1 for every request that failed), to be passed to mla_decode as seq_lens.
+    """
+    tag_types = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+    assert page_tags.dtype in tag_types and page_tags.dim() == 1 and page_tags.is_contiguous()
+    assert block_table.dtype == torch.int32 and block_table.dim() == 2
+    assert block_table.is_contiguous()
+    batch, max_pages = int(block_table.shape[0]), int(block_table.shape[1])
+    assert expected_tags.dtype in tag_types and expected_tags.is_contiguous()
+    assert tuple(expected_tags.shape) == (batch, max_pages)
+    assert seq_lens.dtype == torch.int32 and seq_lens.numel() == batch
+    assert request_status.dtype in tag_types and request_status.numel() == batch
+    assert checked_seq_lens.dtype == torch.int32 and checked_seq_lens.numel() == batch
+    st = load_library().mla_kv_check(_ptr(page_tags), int(page_tags.numel()), _ptr(block_table),
+                                     _ptr(expected_tags), max_pages, _ptr(seq_lens), batch, 64,
+                                     _ptr(request_status), _ptr(checked_seq_lens),
+                                     _stream(stream))
+    _check(st, "mla_kv_check")
 
 
 def mla_decode_static_scratch(q: torch.Tensor, kv_pages: torch.Tensor,

@@ -74,88 +74,97 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ out_base, in
 }
 
 // Merge of mla_decode's pieces. One block per (row, head, quarter of the 512 dims):
-// the 8 warps take every 8th piece and each lane 4 consecutive dims, with 8
-// pieces per warp in flight; the warps then add their sums in shared memory.
+// the 8 warps take every 8th piece and each lane 4 consecutive dims. A warp loads
+// the lse, error flag and output slice of up to kInFlight pieces at once (one
+// pass covers 160 pieces, more than one CTA per SM produces on 152 SMs) and keeps
+// a running maximum, so the merge costs one dependent round of loads after the
+// row table; the warps' sums are then brought to the block's maximum.
 constexpr int kPieceThreads = 256;
 constexpr int kPieceWarps = kPieceThreads / 32;
 constexpr int kQuarters = 4;
-constexpr int kInFlight = 8;  // pieces per warp with loads in flight
+constexpr int kInFlight = 20;  // pieces per warp with loads in flight
 
 __global__ void __launch_bounds__(kPieceThreads)
 combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __restrict__ row_np,
                       const int32_t* __restrict__ piece_err, const float* __restrict__ part_lse,
                       const float* __restrict__ part_out, int heads,
                       __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+  // launched as a dependent of the decode kernel: its partials are visible after this
+  griddep_wait();
+  griddep_launch_dependents();
   __shared__ float4 s_acc[kPieceWarps][32];
-  __shared__ float s_red[kPieceWarps];
-  __shared__ int s_bad;
+  __shared__ float s_m[kPieceWarps], s_w[kPieceWarps];
   const int64_t blk = blockIdx.x;
   const int quarter = (int)(blk % kQuarters);
   const int64_t rh = blk / kQuarters;
   const int r = (int)(rh / heads);
   const int h = (int)(rh - (int64_t)r * heads);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) s_bad = 0;
-  __syncthreads();
   const int np = row_np[r];
   const int base = row_base[r];
-  for (int s = tid; s < np; s += kPieceThreads)
-    if (piece_err[base + s]) s_bad = 1;
-  // max of the pieces' lse
-  float m = -INFINITY;
-  for (int s = tid; s < np; s += kPieceThreads)
-    m = fmaxf(m, part_lse[(int64_t)(base + s) * heads + h]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) s_red[warp] = m;
-  __syncthreads();
-  m = s_red[0];
-#pragma unroll
-  for (int w = 1; w < kPieceWarps; ++w) m = fmaxf(m, s_red[w]);
-  const bool empty = np <= 0 || s_bad || !(m > -INFINITY);
-  __syncthreads();
-  // weighted sums: warp w takes pieces w, w+8, ...; lane takes dims [4*lane, 4*lane+4)
+  const int64_t dim0 = 128 * quarter + 4 * lane;
+  // per warp (identical in every lane): running max m, sum of exp(lse_s - m), and
+  // this lane's sum of exp(lse_s - m) * out_s
+  float m = -INFINITY, wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  if (!empty) {
-    const int64_t dim0 = 128 * quarter + 4 * lane;
-    for (int s0 = warp; s0 < np; s0 += kInFlight * kPieceWarps) {
-      float wgt[kInFlight];
-      float4 v[kInFlight];
+  int bad = 0;
+  for (int s0 = warp; s0 < np; s0 += kInFlight * kPieceWarps) {
+    float l[kInFlight];
+    float4 v[kInFlight];
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) {
+      const int s = s0 + u * kPieceWarps;
+      l[u] = -INFINITY;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s < np) {
+        const int64_t piece = (int64_t)(base + s) * heads + h;
+        l[u] = part_lse[piece];
+        v[u] = *reinterpret_cast<const float4*>(part_out + piece * kDLatent + dim0);
+        bad |= piece_err[base + s];
+      }
+    }
+    float mm = m;
+#pragma unroll
+    for (int u = 0; u < kInFlight; ++u) mm = fmaxf(mm, l[u]);
+    if (mm > -INFINITY) {
+      const float c = m > -INFINITY ? fast_exp2((m - mm) * kLog2e) : 0.f;
+      wsum *= c;
+      acc.x *= c; acc.y *= c; acc.z *= c; acc.w *= c;
 #pragma unroll
       for (int u = 0; u < kInFlight; ++u) {
-        const int s = s0 + u * kPieceWarps;
-        wgt[u] = 0.f;
-        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (s < np) {
-          const int64_t piece = (int64_t)(base + s) * heads + h;
-          const float l = part_lse[piece];
-          wgt[u] = (l > -INFINITY) ? fast_exp2((l - m) * kLog2e) : 0.f;
-          v[u] = *reinterpret_cast<const float4*>(part_out + piece * kDLatent + dim0);
-        }
+        const float w = l[u] > -INFINITY ? fast_exp2((l[u] - mm) * kLog2e) : 0.f;
+        if (w == 0.f) continue;  // empty piece: its output is never read
+        wsum += w;
+        acc.x += w * v[u].x;
+        acc.y += w * v[u].y;
+        acc.z += w * v[u].z;
+        acc.w += w * v[u].w;
       }
-#pragma unroll
-      for (int u = 0; u < kInFlight; ++u) {
-        if (wgt[u] == 0.f) continue;  // empty piece: its output is never read
-        wsum += wgt[u];
-        acc.x += wgt[u] * v[u].x;
-        acc.y += wgt[u] * v[u].y;
-        acc.z += wgt[u] * v[u].z;
-        acc.w += wgt[u] * v[u].w;
-      }
+      m = mm;
     }
   }
   s_acc[warp][lane] = acc;
-  if (lane == 0) s_red[warp] = wsum;
-  __syncthreads();
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_w[warp] = wsum;
+  }
+  const int any_bad = __syncthreads_or(bad);
   if (warp == 0) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kPieceWarps; ++w) M = fmaxf(M, s_m[w]);
+    const bool empty = np <= 0 || any_bad || !(M > -INFINITY);
     float total = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!empty) {
 #pragma unroll
-    for (int w = 0; w < kPieceWarps; ++w) {
-      total += s_red[w];
-      const float4 b = s_acc[w][lane];
-      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+      for (int w = 0; w < kPieceWarps; ++w) {
+        if (!(s_m[w] > -INFINITY)) continue;
+        const float c = fast_exp2((s_m[w] - M) * kLog2e);
+        total += c * s_w[w];
+        const float4 b = s_acc[w][lane];
+        a.x += c * b.x; a.y += c * b.y; a.z += c * b.z; a.w += c * b.w;
+      }
     }
     const float inv = empty ? 0.f : 1.0f / total;
     __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * inv, a.y * inv);
@@ -164,7 +173,7 @@ combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __res
     packed.x = *reinterpret_cast<uint32_t*>(&lo);
     packed.y = *reinterpret_cast<uint32_t*>(&hi);
     *reinterpret_cast<uint2*>(out + rh * kDLatent + 128 * quarter + 4 * lane) = packed;
-    if (quarter == 0 && lane == 0) lse[rh] = empty ? -INFINITY : m + logf(total);
+    if (quarter == 0 && lane == 0) lse[rh] = empty ? -INFINITY : M + logf(total);
   }
 }
 
@@ -187,10 +196,18 @@ cudaError_t launch_combine_pieces(const DecodeWorkspace& ws, int rows, int heads
   (void)max_pieces_per_row;
   const unsigned blocks = (unsigned)((int64_t)rows * heads * kQuarters);
 
-  combine_pieces_kernel<<<blocks, kPieceThreads, 0, stream>>>(
-      ws.row_base, ws.row_np, ws.piece_err, (const float*)ws.part_lse, ws.part_out,
-      heads, out, lse);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(kPieceThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_pieces_kernel, (const int32_t*)ws.row_base,
+                            (const int32_t*)ws.row_np, (const int32_t*)ws.piece_err,
+                            (const float*)ws.part_lse, (const float*)ws.part_out, heads, out,
+                            lse);
 }
 
 }  // namespace mla

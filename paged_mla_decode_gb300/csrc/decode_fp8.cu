@@ -206,8 +206,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- planning (shared by all roles) ----
+  // Shared-memory and TMEM set-up overlap the end of the previous kernel in the
+  // stream; every global access waits for it (griddep_wait).
+  if (warp == kTmaWarp && lane == 0) {
+    tc::prefetch_tensormap(&lat_map);
+    tc::prefetch_tensormap(&rope_map);
+  }
   Plan plan{p.seq_lens, p.batch, p.nq, p.max_pages, kPageSize, p.G, 0};
   if (warp == 0) {
+    griddep_wait();
     const int64_t T = plan_total_tiles_warp(plan);
     if (lane == 0) s_plan[0] = T;
   }
@@ -227,6 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_relinquish();
   }
   __syncthreads();
+  griddep_wait();
+  griddep_launch_dependents();  // the combine kernel may be scheduled (it waits for this grid)
   plan.set_total(s_plan[0]);
   const int c = blockIdx.x;
   const bool works = c < plan.G;
@@ -836,8 +845,15 @@ cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
   p.kv_scale = d.kv_scale;
   p.G = d.G;
   p.ws = d.ws;
-  decode_fp8_kernel<<<d.G, kThreads, kSmemBytes, stream>>>(p, lat_map, rope_map);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)d.G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_fp8_kernel, p, lat_map, rope_map);
 }
 
 }  // namespace mla

@@ -52,6 +52,7 @@ __global__ void kv_append_e4m3_kernel(const __nv_bfloat16* __restrict__ latent,
                                       uint8_t* __restrict__ kv_pages, int64_t num_slots,
                                       float kv_scale) {
   constexpr int kVecPerToken = kDEntry / 8;  // 72
+  griddep_launch_dependents();  // a following decode launch may start its set-up
   int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   int64_t tok = gid / kVecPerToken;
   int v = (int)(gid - tok * kVecPerToken);
@@ -80,6 +81,7 @@ __global__ void kv_append_bf16_kernel(const __nv_bfloat16* __restrict__ latent,
                                       const int32_t* __restrict__ slots, int64_t num_tokens,
                                       __nv_bfloat16* __restrict__ kv_pages, int64_t num_slots) {
   constexpr int kVecPerToken = kDEntry / 8;
+  griddep_launch_dependents();  // a following decode launch may start its set-up
   int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   int64_t tok = gid / kVecPerToken;
   int v = (int)(gid - tok * kVecPerToken);

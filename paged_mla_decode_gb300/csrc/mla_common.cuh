@@ -237,6 +237,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   return r;
 }
 
+// Programmatic dependent launch. griddep_wait() returns once every grid this one
+// depends on has completed and its memory writes are visible (at once when the
+// grid was launched without the programmatic-serialization attribute); it must
+// precede this grid's first global memory access. griddep_launch_dependents()
+// lets the next such grid in the stream be scheduled before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));

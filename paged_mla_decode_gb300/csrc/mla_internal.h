@@ -49,6 +49,16 @@ cudaError_t launch_combine_pieces(const DecodeWorkspace& ws, int rows, int heads
                                   int max_pieces_per_row, __nv_bfloat16* out, float* lse,
                                   cudaStream_t stream);
 
+// Launch attribute that lets a kernel start while the previous kernel in the
+// stream is finishing (programmatic dependent launch); kernels launched with it
+// call griddep_wait() before their first global memory access.
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

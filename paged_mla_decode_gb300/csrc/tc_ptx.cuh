@@ -148,6 +148,11 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // (lane base + i), columns [c, c + 32); thread 16 + i reads the same lane, columns
 // [c + 32, c + 64), where `taddr` carries the lane base (a multiple of 16 inside
 // the warp's quarter) and column c.
+// Brings a kernel-parameter tensor map into the descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void* map) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map))
+               : "memory");
+}
 __device__ __forceinline__ void tmem_ld16x2_32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"

@@ -66,6 +66,12 @@ def test_host_validation_returns_codes(lib):
     assert dec(1, 1, 64) == 1            # null pointers
     assert lib.mla_decode_combine(None, None, 3, 0, None, None, None) == 0
     assert lib.mla_decode_combine(None, None, 3, 5, None, None, None) == 1
+    # integrity check: bad sizes, page size, missing buffers; empty batch is a no-op
+    assert lib.mla_kv_check(None, 10, None, None, 4, None, -1, 64, None, None, None) == 1
+    assert lib.mla_kv_check(None, -1, None, None, 4, None, 1, 64, None, None, None) == 1
+    assert lib.mla_kv_check(None, 10, None, None, 4, None, 1, 32, None, None, None) == 2
+    assert lib.mla_kv_check(None, 10, None, None, 4, None, 0, 64, None, None, None) == 0
+    assert lib.mla_kv_check(None, 10, None, None, 4, None, 1, 64, None, None, None) == 1
     del args
 
 
