@@ -64,6 +64,10 @@ def _rank_env():
     return rank, world, local
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_PER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -72,6 +76,22 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak(operands: str):
+    """Dense tensor peak (TFLOP/s) for the MMA operand type, and where it came from.
+
+    The measured bf16 burst figure; e4m3 operands (tcgen05 kind::f8f6f4) take it
+    times the nominal fp8/bf16 ratio.
+    """
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16, src = float(json.load(f)["bf16_tflops"]), "measured bf16_tflops"
+    except Exception:
+        bf16, src = FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
+    if operands == "fp8":
+        return bf16 * FP8_PER_BF16, f"{src} x {FP8_PER_BF16:g} (nominal fp8/bf16)"
+    return bf16, src
 
 
 def slowest_rank_ms(elapsed_ms, dist=None):
@@ -469,12 +489,25 @@ def run_gpu(args):
     peak, peak_kind = measured_peaks()
     decode_bytes = sb["total"]
     achieved = decode_bytes / (decode_us * 1e-6) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": _profile_traffic(),
+    traffic = _profile_traffic() if args.config == "long" and args.operands == "fp8" else None
+    roof_hbm = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
                 "kernel": "mla_decode call (split decode kernel + LSE combine kernel)",
                 "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
                 "measured" else "fallback 6.8 TB/s",
                 "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_us": decode_us}
+    # the contraction's own roofline: algorithmic flops of the call over the dense
+    # tensor peak of its operand type; the bound is whichever takes longer at peak
+    operands = "bf16" if kv_dtype == "bf16" else args.operands
+    flops = accounting.step_flops(w.seq_lens, Q, H)
+    tpeak, tsrc = tensor_peak(operands)
+    tflops = flops / (decode_us * 1e-6) / 1e12
+    roof_tc = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
+               "frac": tflops / tpeak, "traffic": traffic,
+               "kernel": roof_hbm["kernel"], "peak_source": tsrc,
+               "algorithmic_flops_per_launch": flops, "avg_launch_us": decode_us}
+    tensor_bound = flops / (tpeak * 1e12) > decode_bytes / (peak * 1e9)
+    roofline, roofline_other = (roof_tc, roof_hbm) if tensor_bound else (roof_hbm, roof_tc)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -498,7 +531,11 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}"},
             "steps_per_s": world * steps_per_s, "tokens_per_s": tokens_per_s,
             "kv_gbs": kv_gbs, "pct_of_hbm_peak": 100.0 * kv_gbs / peak,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "kv_check": kv_check,
+            "roofline": roofline,
+            ("roofline_hbm" if tensor_bound else "roofline_tensor"): roofline_other,
+            "logical_kv_gbs": world * accounting.step_bytes(w.seq_lens, Q, H, kv_dtype)["kv"]
+            * steps_per_s / 1e9,
+            "cpu_baseline": cpu, "e2e": e2e, "kv_check": kv_check,
             # per step: KV append, decode and combine
             "gpu_launches": 3 * args.steps, "clocks": clocks,
             "device_status": status,
