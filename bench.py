@@ -177,6 +177,28 @@ def _profile_traffic():
     return prof.get("dram_bytes_per_launch")
 
 
+def rooflines(nbytes, flops, launch_us, hbm_peak, hbm_src, tc_peak, tc_src, traffic=None):
+    """The call's HBM and tensor rooflines; the first one returned is the bound.
+
+    ``nbytes`` and ``flops`` are the algorithmic bytes and flops of one call,
+    ``launch_us`` its measured duration; the bound is the resource that needs
+    the longer time at its peak (HBM GB/s, tensor TFLOP/s).
+    """
+    kernel = "mla_decode call (split decode kernel + LSE combine kernel)"
+    gbs = nbytes / (launch_us * 1e-6) / 1e9
+    tfs = flops / (launch_us * 1e-6) / 1e12
+    hbm = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+           "frac": gbs / hbm_peak, "traffic": traffic, "kernel": kernel,
+           "peak_source": hbm_src, "algorithmic_bytes_per_launch": nbytes,
+           "avg_launch_us": launch_us}
+    tc = {"bound": "tensor", "achieved": tfs, "peak": tc_peak, "unit": "TFLOP/s",
+          "frac": tfs / tc_peak, "traffic": traffic, "kernel": kernel, "peak_source": tc_src,
+          "algorithmic_flops_per_launch": flops, "avg_launch_us": launch_us}
+    if flops / (tc_peak * 1e12) > nbytes / (hbm_peak * 1e9):
+        return tc, hbm
+    return hbm, tc
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle timing (the reference arm and the cpu_baseline field)
 # ---------------------------------------------------------------------------
@@ -490,24 +512,15 @@ def run_gpu(args):
     decode_bytes = sb["total"]
     achieved = decode_bytes / (decode_us * 1e-6) / 1e9
     traffic = _profile_traffic() if args.config == "long" and args.operands == "fp8" else None
-    roof_hbm = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "kernel": "mla_decode call (split decode kernel + LSE combine kernel)",
-                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
-                "measured" else "fallback 6.8 TB/s",
-                "algorithmic_bytes_per_launch": decode_bytes, "avg_launch_us": decode_us}
-    # the contraction's own roofline: algorithmic flops of the call over the dense
-    # tensor peak of its operand type; the bound is whichever takes longer at peak
     operands = "bf16" if kv_dtype == "bf16" else args.operands
     flops = accounting.step_flops(w.seq_lens, Q, H)
     tpeak, tsrc = tensor_peak(operands)
-    tflops = flops / (decode_us * 1e-6) / 1e12
-    roof_tc = {"bound": "tensor", "achieved": tflops, "peak": tpeak, "unit": "TFLOP/s",
-               "frac": tflops / tpeak, "traffic": traffic,
-               "kernel": roof_hbm["kernel"], "peak_source": tsrc,
-               "algorithmic_flops_per_launch": flops, "avg_launch_us": decode_us}
-    tensor_bound = flops / (tpeak * 1e12) > decode_bytes / (peak * 1e9)
-    roofline, roofline_other = (roof_tc, roof_hbm) if tensor_bound else (roof_hbm, roof_tc)
+    roofline, roofline_other = rooflines(
+        decode_bytes, flops, decode_us, peak,
+        f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+        else "fallback 6.8 TB/s", tpeak, tsrc, traffic)
+    tensor_bound = roofline["bound"] == "tensor"
+    del achieved
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -70,3 +70,28 @@ def test_reference_arm_other_ranks_exit_without_work():
     p.join(timeout=60)
     assert p.exitcode == 0
     assert out.get(timeout=10) == (1, 0)
+
+
+def test_roofline_bound_follows_the_longer_time():
+    """The long-context call is HBM-bound, the 4-draft speculative call tensor-bound
+    (at the fp8 peak), from the algorithmic bytes and flops of the workloads."""
+    import bench
+    from paged_mla_decode_gb300 import accounting
+    from paged_mla_decode_gb300 import workloads as wl
+
+    hbm, _ = bench.measured_peaks()
+    fp8, _ = bench.tensor_peak("fp8")
+    bf16, _ = bench.tensor_peak("bf16")
+    assert fp8 == 2 * bf16
+    for make, bound in ((wl.long_context, "hbm"), (wl.speculative, "tensor")):
+        w = make()
+        nbytes = accounting.step_bytes(w.seq_lens, w.num_queries, w.num_heads, "e4m3",
+                                       unique_tokens=w.unique_tokens)["total"]
+        flops = accounting.step_flops(w.seq_lens, w.num_queries, w.num_heads)
+        first, other = bench.rooflines(nbytes, flops, 100.0, hbm, "m", fp8, "m")
+        assert first["bound"] == bound and other["bound"] != bound
+        # achieved = algorithmic work / time; frac = achieved / peak
+        assert abs(first["frac"] - first["achieved"] / first["peak"]) < 1e-12
+    # a call that takes exactly the HBM time at peak reads 1.0 of the HBM roofline
+    first, _ = bench.rooflines(6.76e9, 1.0, 1000.0, 6760.0, "m", fp8, "m")
+    assert first["bound"] == "hbm" and abs(first["frac"] - 1.0) < 1e-9
