@@ -95,3 +95,25 @@ def test_roofline_bound_follows_the_longer_time():
     # a call that takes exactly the HBM time at peak reads 1.0 of the HBM roofline
     first, _ = bench.rooflines(6.76e9, 1.0, 1000.0, 6760.0, "m", fp8, "m")
     assert first["bound"] == "hbm" and abs(first["frac"] - 1.0) < 1e-9
+
+
+def test_reference_arm_line_has_the_contract_keys(capsys, monkeypatch):
+    """`bench.py --impl reference` (the float64 oracle on the host cores) prints one
+    JSON line with the keys the driver reads; checked on the tiny workload."""
+    import json
+
+    import bench
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.main(["--impl", "reference", "--config", "tiny", "--steps", "1",
+                       "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["e2e"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
