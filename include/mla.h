@@ -41,6 +41,10 @@
  *    sticky bit is set in the status word at the start of the workspace
  *    (MLA_DEVICE_ERR_*), which the caller may read back at any time.
  *  - Entry points are re-entrant and keep no global state.
+ *  - Stream order is kept: mla_decode's kernels are launched with programmatic
+ *    dependent launch (they may become resident while the previous kernel in
+ *    the stream finishes) but each waits for all earlier work in the stream to
+ *    complete before its first memory access.
  */
 #ifndef PAGED_MLA_DECODE_MLA_H_
 #define PAGED_MLA_DECODE_MLA_H_
