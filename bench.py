@@ -510,7 +510,6 @@ def run_gpu(args):
 
     peak, peak_kind = measured_peaks()
     decode_bytes = sb["total"]
-    achieved = decode_bytes / (decode_us * 1e-6) / 1e9
     traffic = _profile_traffic() if args.config == "long" and args.operands == "fp8" else None
     operands = "bf16" if kv_dtype == "bf16" else args.operands
     flops = accounting.step_flops(w.seq_lens, Q, H)
@@ -520,7 +519,6 @@ def run_gpu(args):
         f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
         else "fallback 6.8 TB/s", tpeak, tsrc, traffic)
     tensor_bound = roofline["bound"] == "tensor"
-    del achieved
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
