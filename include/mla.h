@@ -40,7 +40,9 @@
  *    the affected (request, draft) rows get out = 0 and lse = -inf, and a
  *    sticky bit is set in the status word at the start of the workspace
  *    (MLA_DEVICE_ERR_*), which the caller may read back at any time.
- *  - Entry points are re-entrant and keep no global state.
+ *  - Entry points are re-entrant and keep no global state, with one
+ *    exception: mla_decode_static_scratch keeps its scratch in one array per
+ *    device, shared by all of its calls (see its declaration).
  *  - Stream order is kept: mla_decode's kernels are launched with programmatic
  *    dependent launch (they may become resident while the previous kernel in
  *    the stream finishes) but each waits for all earlier work in the stream to
@@ -272,16 +274,21 @@ MLA_API mla_status mla_kv_check(const uint32_t* page_tags, int64_t num_pages,
  *    more scratch than MLA_STATIC_SCRATCH_BYTES, i.e. when
  *    mla_decode_workspace_size(batch, num_queries, num_heads, num_ctas) exceeds
  *    it: at 64 heads with one CTA per SM on a 152-SM GPU, batch x num_queries
- *    may be at most 358 rows.
+ *    may be at most 229 rows.
  *  - Set-up: the first call on each device looks up the array's device address
  *    with that device current (cudaGetSymbolAddress). Make that first call
- *    before any stream capture.
+ *    before any stream capture. The address is kept per device ordinal and
+ *    belongs to the runtime's primary context of that device: the entry point
+ *    assumes that context for the whole process (no context of the caller's
+ *    own, no cudaDeviceReset between calls).
  *  - Sharing: every call on a device uses the same array, which keeps the last
  *    call's contents. Calls that overlap on the GPU (for instance on two
  *    streams) race and give wrong results: order them on one stream or with
  *    events.
  *  - device_status: optional device pointer (may be NULL) that receives this
- *    call's MLA_DEVICE_ERR_* bits; the copy in the array is cleared afterwards.
+ *    call's MLA_DEVICE_ERR_* bits; the copy in the array is cleared afterwards,
+ *    also when the call returns MLA_ERR_CUDA after some of its work was
+ *    enqueued (the first error is returned).
  */
 #define MLA_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 MLA_API mla_status mla_decode_static_scratch(const void* q, const void* kv_pages, int64_t num_pages,

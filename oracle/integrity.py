@@ -11,7 +11,7 @@ mappings are compared, and a request with any mismatch is aborted instead of
 being allowed to return data computed from a page that is no longer its own.
 The check runs as a separate batch pass, not inside the attention kernel.
 
-Readings where the page gives no layout (each one is listed in the design doc):
+Readings where the page gives no layout (this module's own choices):
 
 * a tag is a 32-bit unsigned integer per physical page (``page_tags[p]``);
 * a request's expected tags sit beside its block-table entries, one per logical

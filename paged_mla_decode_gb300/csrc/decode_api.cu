@@ -83,6 +83,8 @@ mla_status decode_impl(const void* q, const void* kv_pages, int64_t num_pages, i
   p.ws.piece_err = reinterpret_cast<int32_t*>(ws + L.piece_err);
   p.ws.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   p.ws.part_out = reinterpret_cast<float*>(ws + L.part_out);
+  p.ws.q_op = ws + L.q_op;
+  p.ws.q_mul = reinterpret_cast<float*>(ws + L.q_mul);
 
   if (!p.bf16 && num_pages > (int64_t)(0x7fffffff / kPageSize)) return MLA_ERR_UNSUPPORTED;
 

@@ -13,7 +13,9 @@
 // q (bf16) is scaled per head by a power of two (max |q| in [2^7, 2^8)) and split
 // into two e4m3 terms q_hi = e4m3(q), q_lo = e4m3(q - q_hi), which is exact for
 // bf16 inputs (8 significant bits = 4 + 4) down to 2^-10 of the head's max, so
-// S_hi + S_lo is q . k up to fp32 accumulation. P = 2^(s - m + 6) is split into
+// S_hi + S_lo is q . k up to fp32 accumulation. The split runs once per row in a
+// small kernel launched before the decode kernel (q_split_kernel), which writes
+// the A operand in the order the decode kernel's threads load it. P = 2^(s - m + 6) is split into
 // an e4m3 term and an e5m2 remainder (7 significant bits; the e5m2 range keeps
 // tokens down to 2^-24 of the running maximum). All heads attend over the one latent
 // head ("vLLM x AgentX", section "Kimi K3"), so one page serves 64 heads, and V
@@ -21,7 +23,7 @@
 // serve trillions of tokens ...", section "First, understand the workload").
 //
 // Warp roles (224 threads):
-//   warps 0-3  q staging, softmax and epilogue. Row t of A and S is (head
+//   warps 0-3  q loading, softmax and epilogue. Row t of A and S is (head
 //              16*(t/32) + t%16, part (t/16)%2), part 0 = hi, 1 = lo. Thread t
 //              handles head 16*(t/32) + t%16 and tokens 32*((t/16)%2) .. +31 of a
 //              page: it reads both terms' rows of its half-page (a half-split
@@ -37,7 +39,7 @@
 // O^T [256,512). The rope part of A is in shared memory.
 //
 // Every wait is bounded (2 s); on timeout the CTA records MLA_DEVICE_ERR_TIMEOUT,
-// stops, drains its MMAs and copies (bounded) and frees TMEM.
+// stops, drains its MMAs and copies (bounded, 2 s) and frees TMEM.
 #include <atomic>
 
 #include <cuda.h>
@@ -61,7 +63,14 @@ constexpr int kRopeOff = 4 * kLatBlock;              // rope block within a page
 constexpr int kPBytes = 64 * 128;                    // P^T: 64 heads x [64 hi | 64 lo]
 constexpr int kPOffset = 6;                          // P = 2^(s - m + 6)
 constexpr float kRescaleThresh = 2.8f;               // P <= 2^8.8 < 448 (e4m3 max)
-constexpr uint64_t kWaitNs = 2000000000ull;
+// Limit of a wait on another role of the pipeline, and of a wait for copies and
+// MMAs already issued (the drain before exit). A test build lowers the first
+// (MLA_PIPELINE_WAIT_NS) to make the timeout path run; the drain keeps 2 s.
+#ifndef MLA_PIPELINE_WAIT_NS
+#define MLA_PIPELINE_WAIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitNs = MLA_PIPELINE_WAIT_NS;
+constexpr uint64_t kDrainWaitNs = 2000000000ull;
 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kQCol = 0;
@@ -93,7 +102,15 @@ constexpr int BAR_Q_READY = 2 * kRing + 11;   // (4 softmax warps)
 constexpr int BAR_Q_EMPTY = 2 * kRing + 12;
 constexpr int BAR_DRAIN = 2 * kRing + 13;      // [2] QK warp, PV warp
 constexpr int BAR_P_EMPTY = 2 * kRing + 15;    // [kPBufs] PV of page j read P buffer j % 3
+#ifdef MLA_TEST_STALL_QK
+// Test build only: a barrier that nothing ever completes. The QK issuer waits on
+// it before its third page, so the wait runs out and the CTA takes the timeout
+// path (stop every role, drain the copies and MMAs in flight, free TMEM).
+constexpr int BAR_TEST_STALL = 2 * kRing + 15 + kPBufs;
+constexpr int kNumBars = BAR_TEST_STALL + 1;
+#else
 constexpr int kNumBars = 2 * kRing + 15 + kPBufs;
+#endif
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024 alignment
@@ -206,15 +223,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // ---- planning (shared by all roles) ----
-  // Shared-memory and TMEM set-up overlap the end of the previous kernel in the
-  // stream; every global access waits for it (griddep_wait).
+  // This kernel starts once the query split kernel before it has passed its own
+  // wait for all earlier work in the stream (see launch_decode_fp8), so the
+  // lengths, block table and pages may be read at once; only the split query
+  // itself needs the split kernel to have completed (griddep_wait before q_op).
   if (warp == kTmaWarp && lane == 0) {
     tc::prefetch_tensormap(&lat_map);
     tc::prefetch_tensormap(&rope_map);
   }
   Plan plan{p.seq_lens, p.batch, p.nq, p.max_pages, kPageSize, p.G, 0};
   if (warp == 0) {
-    griddep_wait();
     const int64_t T = plan_total_tiles_warp(plan);
     if (lane == 0) s_plan[0] = T;
   }
@@ -234,7 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_relinquish();
   }
   __syncthreads();
-  griddep_wait();
   griddep_launch_dependents();  // the combine kernel may be scheduled (it waits for this grid)
   plan.set_total(s_plan[0]);
   const int c = blockIdx.x;
@@ -335,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // no copy may land after the CTA exits: wait for the last issued pages
         for (int64_t jj = j > kRing ? j - kRing : 0; jj < j; ++jj)
           tc::mbar_wait(bar(BAR_PAGE_FULL + (int)(jj % kRing)), (uint32_t)(jj / kRing) & 1,
-                        kWaitNs);
+                        kDrainWaitNs);
       }
       __syncwarp();
     } else if (warp == kQkWarp || warp == kPvWarp) {
@@ -363,6 +380,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+#ifdef MLA_TEST_STALL_QK
+          if (k == 2) {
+            ok = wait0(BAR_TEST_STALL, 0);
+            if (!ok) break;
+          }
+#endif
           const int slot = (int)(k % kRing);
           const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
           ok = wait0(BAR_PAGE_FULL + slot, (uint32_t)(k / kRing) & 1);
@@ -455,7 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // drain: every MMA this thread issued has finished before TMEM is freed
         const int db = BAR_DRAIN + (warp == kPvWarp ? 1 : 0);
         tc::mma_commit(bar(db));
-        if (!tc::mbar_wait(bar(db), 0, kWaitNs)) atomicOr(p.ws.status, MLA_DEVICE_ERR_TIMEOUT);
+        if (!tc::mbar_wait(bar(db), 0, kDrainWaitNs))
+          atomicOr(p.ws.status, MLA_DEVICE_ERR_TIMEOUT);
       }
       __syncwarp();
     } else {
@@ -484,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ps = d0.flags & kDescPieceStart;
         }
         if (ps) {
-          // ---- stage q of this row: per-head power-of-two scale, e4m3 hi/lo split ----
+          // ---- load the split q of this row into A ----
           if (piece > 0) {
             const bool got = tc::mbar_wait(bar(BAR_Q_EMPTY), (uint32_t)(piece - 1) & 1, kWaitNs);
             if (named_bar_softmax_or(!got || flags[F_ABORT])) {
@@ -492,113 +516,37 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
           }
-          // This thread reads half of its head's 576 dims (part 0: 0-287, part 1:
-          // 288-575) in one batch; the head's max |q| comes from the partner lane.
+          // The query split kernel wrote this row's operand as [36 chunks][128 lanes]
+          // [16 codes]: this thread loads the 36 chunks of its own lane (coalesced
+          // across the warp), stores the 32 latent chunks into its TMEM lane and the
+          // 4 rope chunks into its shared-memory row (64-byte swizzle).
+          griddep_wait();  // the split kernel has completed and its writes are visible
           const bool live = h < H;
-          const uint4* qh = reinterpret_cast<const uint4*>(
-                                p.q + ((int64_t)row * H + (live ? h : 0)) * kDEntry) +
-                            36 * part;
-          // max pass over all 36 vectors; round 0's 12 stay in registers, rounds 1
-          // and 2 are read again (from L2) while the previous round converts
-          uint4 w[2][12];
-          float amax = 0.f;
-          {
-            uint4 a[36];
+          qmul = live ? __ldcg(p.ws.q_mul + (int64_t)row * 64 + h) : 0.f;
+          const uint4* src =
+              reinterpret_cast<const uint4*>(p.ws.q_op + (int64_t)row * kQOpRowBytes) + t;
+          uint4 qc[kQOpChunks];
 #pragma unroll
-            for (int u = 0; u < 36; ++u) a[u] = live ? __ldg(qh + u) : make_uint4(0, 0, 0, 0);
+          for (int u = 0; u < kQOpChunks; ++u)
+            qc[u] = live ? __ldcg(src + 128 * u) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-            for (int u = 0; u < 36; ++u) {
-              const uint32_t ws[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+          for (int g = 0; g < 4; ++g) {
+            uint32_t v[32];
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float2 f =
-                    __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
-                amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-              }
+            for (int k = 0; k < 8; ++k) {
+              v[4 * k] = qc[8 * g + k].x;
+              v[4 * k + 1] = qc[8 * g + k].y;
+              v[4 * k + 2] = qc[8 * g + k].z;
+              v[4 * k + 3] = qc[8 * g + k].w;
             }
-#pragma unroll
-            for (int u = 0; u < 12; ++u) w[0][u] = a[u];
+            tc::tmem_st32(tmem + lane_base + kQCol + 32 * g, v);
           }
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 16));
-          int shift = 0;
-          if (amax > 0.f && isfinite(amax)) {
-            int e;
-            frexpf(amax, &e);
-            shift = 8 - e;  // scaled max in [2^7, 2^8)
-          }
-          const float sc = live ? ldexpf(1.0f, shift) : 0.f;
-          qmul = live ? p.score_mul * ldexpf(1.0f, -shift) : 0.f;
-          // Three rounds of 96 dims per thread through the (free) P buffers: each
-          // thread writes the hi codes of its dims to its head's hi row and the lo
-          // codes to the lo row ([128 rows][own 96 B | partner 96 B]), then copies
-          // its own row's 48 words into place: words [24r, 24r+24) and [72+24r, ...)
-          // (word i = codes of dims 4i..4i+3; words 128-143 are the rope).
-          uint8_t* stage = smem + kOffP;
-          const int t_hi = 32 * warp + (lane & 15);
 #pragma unroll
-          for (int r = 0; r < 3; ++r) {
-            if (r < 2) {
-#pragma unroll
-              for (int u = 0; u < 12; ++u)
-                w[(r + 1) & 1][u] = live ? __ldg(qh + 12 * (r + 1) + u) : make_uint4(0, 0, 0, 0);
-            }
-#pragma unroll
-            for (int u2 = 0; u2 < 6; ++u2) {  // 16 dims -> one 16-byte vector of each term
-              uint32_t hw[4], lw[4];
-#pragma unroll
-              for (int half = 0; half < 2; ++half) {
-                const uint4 wv = w[r & 1][2 * u2 + half];
-                const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-                uint32_t hc[4], lc[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const float2 f =
-                      __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
-                  const float x0 = f.x * sc, x1 = f.y * sc;
-                  hc[k] = e4m3x2_of(x0, x1);
-                  const float2 hv = e4m3x2_value(hc[k]);
-                  lc[k] = e4m3x2_of(x0 - hv.x, x1 - hv.y);
-                }
-                hw[2 * half] = hc[0] | (hc[1] << 16);
-                hw[2 * half + 1] = hc[2] | (hc[3] << 16);
-                lw[2 * half] = lc[0] | (lc[1] << 16);
-                lw[2 * half + 1] = lc[2] | (lc[3] << 16);
-              }
-              const int off = 96 * part + 16 * u2;
-              *reinterpret_cast<uint4*>(stage + t_hi * 192 + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-              *reinterpret_cast<uint4*>(stage + (t_hi + 16) * 192 + off) =
-                  make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
-            named_bar_softmax();  // the round's rows are complete
-            const uint32_t* mine = reinterpret_cast<const uint32_t*>(stage + t * 192);
-#pragma unroll
-            for (int g = 0; g < 3; ++g) {  // own dims [96r, 96r+96): TMEM words 24r + 8g
-              uint32_t v8[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v8[i] = mine[8 * g + i];
-              tc::tmem_st8(tmem + lane_base + kQCol + 24 * r + 8 * g, v8);
-            }
-#pragma unroll
-            for (int g = 0; g < 3; ++g) {  // dims [288+96r, ...): words 72 + 24r + 8g
-              uint32_t v8[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v8[i] = mine[24 + 8 * g + i];
-              const int word = 72 + 24 * r + 8 * g;
-              if (word < 128) {
-                tc::tmem_st8(tmem + lane_base + kQCol + word, v8);
-              } else {  // rope: shared memory row t (64 B, 64-byte swizzle)
-                const int u0 = (word - 128) / 4;
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                  const uint32_t a =
-                      sbase + kOffQRope + t * 64 + (((u0 + h2) ^ ((t >> 1) & 3)) << 4);
-                  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a),
-                               "r"(v8[4 * h2]), "r"(v8[4 * h2 + 1]), "r"(v8[4 * h2 + 2]),
-                               "r"(v8[4 * h2 + 3]));
-                }
-              }
-            }
-            named_bar_softmax();  // the staging rows are free again
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const uint32_t a = sbase + kOffQRope + t * 64 + ((c4 ^ ((t >> 1) & 3)) << 4);
+            const uint4 v = qc[32 + c4];
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(v.x), "r"(v.y),
+                         "r"(v.z), "r"(v.w));
           }
           tc::tmem_wait_st();
           tc::fence_proxy_async_smem();
@@ -793,6 +741,85 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kQkWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---- query split: once per (request, draft) row, before the decode kernel ----
+// q (bf16) of head h is scaled by 2^shift (max |q| of the head in [2^7, 2^8)) and
+// split into q_hi = e4m3(q * 2^shift) and q_lo = e4m3(q * 2^shift - q_hi): exact
+// for bf16 inputs down to 2^-10 of the head's max. The codes are written as the
+// decode kernel's A operand: row t of A (t < 128) is head 16*(t/32) + t%16, term
+// (t/16)%2 (0 = hi, 1 = lo), stored as q_op[row][u][t][16] for the 36 chunks u of
+// 16 dims; q_mul[row][h] = score multiplier * 2^-shift. A block handles 8 heads of
+// one row, one 16-dim chunk per thread.
+constexpr int kSplitHeads = 8;
+constexpr int kSplitThreads = kSplitHeads * kQOpChunks;  // 288
+
+__global__ void __launch_bounds__(kSplitThreads)
+    q_split_kernel(const __nv_bfloat16* __restrict__ q, int heads, float score_mul,
+                   uint8_t* __restrict__ q_op, float* __restrict__ q_mul) {
+  // All earlier work in the stream has completed once this returns; the decode
+  // kernel that follows may start only after every block has passed it.
+  griddep_wait();
+  griddep_launch_dependents();
+  __shared__ unsigned s_amax[kSplitHeads];
+  const int tid = threadIdx.x;
+  const int hl = tid / kQOpChunks, u = tid - hl * kQOpChunks;
+  const int groups = (heads + kSplitHeads - 1) / kSplitHeads;
+  const int64_t row = blockIdx.x / groups;
+  const int h = (int)(blockIdx.x - row * groups) * kSplitHeads + hl;
+  const bool live = h < heads;
+  if (tid < kSplitHeads) s_amax[tid] = 0u;
+  uint4 a[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+  if (live) {
+    const uint4* src = reinterpret_cast<const uint4*>(q + (row * heads + h) * kDEntry) + 2 * u;
+    a[0] = __ldg(src);
+    a[1] = __ldg(src + 1);
+  }
+  float f[16];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t ws[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 v = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[k]));
+      f[8 * i + 2 * k] = v.x;
+      f[8 * i + 2 * k + 1] = v.y;
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+  __syncthreads();
+  atomicMax(&s_amax[hl], __float_as_uint(amax));  // non-negative: integer order = float order
+  __syncthreads();
+  if (!live) return;
+  amax = __uint_as_float(s_amax[hl]);
+  int shift = 0;
+  if (amax > 0.f && isfinite(amax)) {
+    int e;
+    frexpf(amax, &e);
+    shift = 8 - e;  // scaled max in [2^7, 2^8)
+  }
+  const float sc = ldexpf(1.0f, shift);
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t hc[2], lc[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float x0 = f[4 * k + 2 * e] * sc, x1 = f[4 * k + 2 * e + 1] * sc;
+      hc[e] = e4m3x2_of(x0, x1);
+      const float2 hv = e4m3x2_value(hc[e]);
+      lc[e] = e4m3x2_of(x0 - hv.x, x1 - hv.y);
+    }
+    hw[k] = hc[0] | (hc[1] << 16);
+    lw[k] = lc[0] | (lc[1] << 16);
+  }
+  const int lane_hi = 32 * (h >> 4) + (h & 15);
+  uint4* dst = reinterpret_cast<uint4*>(q_op + row * kQOpRowBytes) + 128 * u;
+  dst[lane_hi] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  dst[lane_hi + 16] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  if (u == 0) q_mul[row * 64 + h] = score_mul * ldexpf(1.0f, -shift);
+}
+
 }  // namespace
 
 cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
@@ -845,12 +872,24 @@ cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
   p.kv_scale = d.kv_scale;
   p.G = d.G;
   p.ws = d.ws;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  {
+    const int groups = (d.heads + kSplitHeads - 1) / kSplitHeads;
+    cudaLaunchConfig_t sc = {};
+    sc.gridDim = dim3((unsigned)((int64_t)d.batch * d.nq * groups));
+    sc.blockDim = dim3(kSplitThreads);
+    sc.stream = stream;
+    sc.attrs = attr;
+    sc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&sc, q_split_kernel, d.q, d.heads, d.score_mul,
+                                       d.ws.q_op, d.ws.q_mul);
+    if (e != cudaSuccess) return e;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)d.G);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_fp8_kernel, p, lat_map, rope_map);

@@ -59,15 +59,19 @@ extern "C" mla_status mla_decode_static_scratch(
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // The row table and partials are rewritten by every call; only the status word
   // must start at zero. It is zero when the array is loaded and is cleared after
-  // each call (once copied out), so a call that fails its checks enqueues nothing.
+  // each call (once copied out). A call that fails its host checks enqueues
+  // nothing; MLA_ERR_CUDA may come after a kernel was enqueued, so the copy and
+  // the clear are enqueued for it too and the first error is returned.
   st = mla_decode(q, kv_pages, num_pages, page_size, kv_dtype, block_table, max_pages, seq_lens,
                   batch, num_queries, num_heads, sm_scale, kv_scale, num_ctas, scratch,
                   kScratchBytes, out, lse, stream);
-  if (st != MLA_OK) return st;
+  if (st != MLA_OK && st != MLA_ERR_CUDA) return st;
   if (device_status != nullptr &&
       cudaMemcpyAsync(device_status, scratch, sizeof(unsigned), cudaMemcpyDeviceToDevice, s) !=
-          cudaSuccess)
-    return MLA_ERR_CUDA;
-  if (cudaMemsetAsync(scratch, 0, sizeof(unsigned), s) != cudaSuccess) return MLA_ERR_CUDA;
-  return MLA_OK;
+          cudaSuccess &&
+      st == MLA_OK)
+    st = MLA_ERR_CUDA;
+  if (cudaMemsetAsync(scratch, 0, sizeof(unsigned), s) != cudaSuccess && st == MLA_OK)
+    st = MLA_ERR_CUDA;
+  return st;
 }

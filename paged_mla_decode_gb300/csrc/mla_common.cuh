@@ -31,12 +31,17 @@ constexpr float kLn2 = 0.6931471805599453f;
 //   piece_err int32[P]       1 if the piece met a bad page id
 //   part_lse  float[P][H]    log-sum-exp of each piece (natural log)
 //   part_out  float[P][H][512] normalised partial output of each piece
+//   q_op      uint8[R][36][128][16] the query of each row as the e4m3 operand of
+//                                   the FP8 decode kernel (see decode_fp8.cu)
+//   q_mul     float[R][64]        score multiplier of each (row, head)
 //
 // with R = batch * num_queries rows and P = num_ctas + R an upper bound on the
 // number of pieces (each CTA range adds at most one piece per row boundary).
 // ---------------------------------------------------------------------------
+constexpr int kQOpChunks = kDEntry / 16;               // 36 chunks of 16 dims
+constexpr int kQOpRowBytes = kQOpChunks * 128 * 16;    // 73,728 B per row
 struct WorkspaceLayout {
-  size_t row_base, row_np, piece_err, part_lse, part_out, total;
+  size_t row_base, row_np, piece_err, part_lse, part_out, q_op, q_mul, total;
   int64_t max_pieces;
 };
 
@@ -51,6 +56,8 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int64_t rows, int he
   w.piece_err = off; off = align_up(off + 4 * w.max_pieces, 256);
   w.part_lse = off; off = align_up(off + 4 * w.max_pieces * heads, 256);
   w.part_out = off; off = align_up(off + 4 * w.max_pieces * heads * (int64_t)kDLatent, 256);
+  w.q_op = off; off = align_up(off + (size_t)kQOpRowBytes * rows, 256);
+  w.q_mul = off; off = align_up(off + 4 * 64 * rows, 256);
   w.total = off;
   return w;
 }

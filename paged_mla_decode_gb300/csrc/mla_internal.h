@@ -19,6 +19,8 @@ struct DecodeWorkspace {
   int32_t* piece_err;
   float* part_lse;
   float* part_out;
+  uint8_t* q_op;    // FP8 decode only: the split query operand of each row
+  float* q_mul;     // FP8 decode only: score multiplier of each (row, head)
 };
 
 // Everything a decode kernel launch needs (validated by the caller).
@@ -42,6 +44,8 @@ cudaError_t launch_decode_tensor_core(const DecodeLaunch& d, cudaStream_t stream
 
 // Split-KV decode with the e4m3 cache bytes as tensor-core operands
 // (decode_fp8.cu); e4m3 caches only, heads <= 64, num_pages * 64 < 2^31.
+// Launches the query split (one pass per row into ws.q_op / ws.q_mul), then the
+// decode kernel, which reads it.
 cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream);
 
 // Merge the pieces written by a decode kernel into out (bf16) and lse (fp32).
