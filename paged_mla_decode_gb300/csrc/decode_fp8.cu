@@ -232,11 +232,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::prefetch_tensormap(&rope_map);
   }
   Plan plan{p.seq_lens, p.batch, p.nq, p.max_pages, kPageSize, p.G, 0};
+  const int c = blockIdx.x;
   if (warp == 0) {
-    const int64_t T = plan_total_tiles_warp(plan);
-    if (lane == 0) s_plan[0] = T;
+    // the whole plan in one warp pass: total tiles, then this CTA's first row
+    Plan pl = plan;
+    pl.set_total(plan_total_tiles_warp(pl));
+    const int64_t xb = c < pl.G ? pl.cta_start(c) : 0;
+    RowCursor f = plan_find_row_warp(pl, xb, c == 0, p.ws.row_base, p.ws.row_np, p.ws.status);
+    if (lane == 0) {
+      s_plan[0] = pl.T;
+      s_plan[1] = f.r;
+      s_plan[2] = f.rt;
+      s_plan[3] = f.t;
+      s_plan[4] = f.base;
+      s_plan[5] = f.n;
+    }
   }
-  if (tid == 0) {
+  if (warp == kPvWarp && lane == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       const bool by_warps = (i >= BAR_S_EMPTY && i < BAR_S_EMPTY + 2) ||
                             (i >= BAR_P_FULL && i < BAR_P_FULL + kPBufs) || i == BAR_O_EMPTY ||
@@ -251,27 +263,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc::tmem_relinquish();
   }
-  __syncthreads();
-  griddep_launch_dependents();  // the combine kernel may be scheduled (it waits for this grid)
-  plan.set_total(s_plan[0]);
-  const int c = blockIdx.x;
-  const bool works = c < plan.G;
-  const int64_t x_begin = works ? plan.cta_start(c) : 0;
-  const int64_t x_end = works ? plan.cta_start(c + 1) : 0;
-  if (warp == 0) {
-    RowCursor f = plan_find_row_warp(plan, x_begin, c == 0, p.ws.row_base, p.ws.row_np,
-                                     p.ws.status);
-    if (lane == 0) {
-      s_plan[1] = f.r;
-      s_plan[2] = f.rt;
-      s_plan[3] = f.t;
-      s_plan[4] = f.base;
-      s_plan[5] = f.n;
-    }
-  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  griddep_launch_dependents();  // the combine kernel may be scheduled (it waits for this grid)
+  plan.set_total(s_plan[0]);
+  const bool works = c < plan.G;
+  const int64_t x_begin = works ? plan.cta_start(c) : 0;
+  const int64_t x_end = works ? plan.cta_start(c + 1) : 0;
   const uint32_t tmem = *tmem_slot;
   const RowCursor cur0{(int)s_plan[1], s_plan[2], (int)s_plan[3], (int)s_plan[4],
                        (int)s_plan[5]};
