@@ -149,8 +149,16 @@ MLA_API size_t mla_decode_workspace_size(int batch, int num_queries, int num_hea
  *
  * Arithmetic: for an e4m3 cache the cache bytes themselves are the tensor-core
  * operands (tcgen05 kind::f8f6f4); q is scaled per head by a power of two and
- * split into two e4m3 terms (exact for bf16 q), the softmax weights into an
- * e4m3 and an e5m2 term (7 significant bits); accumulation is fp32. For a bf16
+ * split into two e4m3 terms (exact for bf16 q down to 2^-10 of the head's
+ * largest element); accumulation is fp32. The softmax weights P = 2^(s - m + 6)
+ * (s in log2 units, m a running maximum) are split into an e4m3 and an e5m2
+ * term: relative error at most 2^-7 for P >= 2^-6, coarser below, and P below
+ * about 2^-17 drops out of `out` (the normaliser sums the exact P). m follows
+ * each 64-token page's maximum within [-6, +2.8] (a page further below lowers
+ * m, unless the weight accumulated so far exceeds 2^28 times the page's
+ * largest), so every page's largest P lies in [1, 448]; what a page loses is
+ * confined to its tokens below 2^-6 of its largest weight. Each piece of the
+ * split (one per CTA) has its own maximum; pieces merge in fp32. For a bf16
  * cache both contractions use bf16 operands (kind::f16).
  *
  * q           device, bf16 [batch][num_queries][num_heads][576]

@@ -63,6 +63,14 @@ constexpr int kRopeOff = 4 * kLatBlock;              // rope block within a page
 constexpr int kPBytes = 64 * 128;                    // P^T: 64 heads x [64 hi | 64 lo]
 constexpr int kPOffset = 6;                          // P = 2^(s - m + 6)
 constexpr float kRescaleThresh = 2.8f;               // P <= 2^8.8 < 448 (e4m3 max)
+// A page whose maximum lies more than kLowThresh below the running maximum
+// brings the running maximum down to its own (O^T and l scale up), so that its
+// largest weight is at least 2^(kPOffset - kLowThresh) = 1 and its tokens keep
+// the split's precision, unless the accumulated mass l would then exceed
+// kMassCap (the page's largest weight is then below 2^-28 of the mass so far:
+// 2^18 such tokens still stay below 2^-10 of it).
+constexpr float kLowThresh = 6.0f;
+constexpr float kMassCap = 17179869184.0f;           // 2^34 = 2^(kPOffset + 28)
 // Limit of a wait on another role of the pipeline, and of a wait for copies and
 // MMAs already issued (the drain before exit). A test build lowers the first
 // (MLA_PIPELINE_WAIT_NS) to make the timeout path run; the drain keeps 2 s.
@@ -587,13 +595,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmax = fmaxf(tmax, s[i]);
         }
         tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-        // lazy running max: O is rescaled only when a head's max grows past the threshold
+        // lazy running max: O is rescaled only when a head's page max rises more than
+        // kRescaleThresh above it or falls more than kLowThresh below it
         float alpha = 1.f;
         bool grow = false;
         if (ps) {
           m = tmax;
         } else if (tmax > m + kRescaleThresh) {
           alpha = m == -INFINITY ? 0.f : fast_exp2(m - tmax);
+          m = tmax;
+          l *= alpha;
+          grow = true;
+        } else if (tmax < m - kLowThresh && l * fast_exp2(m - tmax) <= kMassCap) {
+          alpha = fast_exp2(m - tmax);  // > 1: the page is far below the running max
           m = tmax;
           l *= alpha;
           grow = true;
@@ -616,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          // bring O^T (PV of the previous page done) to the new maxima
+          // bring O^T (PV of the previous page done) to the new maxima (up or down)
           const bool got =
               tc::mbar_wait(bar(BAR_PV_DONE + (int)((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1,
                             kWaitNs);

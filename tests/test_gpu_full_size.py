@@ -42,7 +42,14 @@ def _check_sampled(w, pages, dev, samples, kv_dtype="e4m3"):
             n = oatt.visible_length(L, w.num_queries, j)
             q = oe4m3.bf16_bits_to_f64(w.q_bits[b, j])
             ref_out, ref_lse = oatt.attend(q, k[:n], w.sm_scale)
-            assert_close(out[b, j], lse[b, j], ref_out, ref_lse, what=f"{w.name} b={b} j={j}")
+            _, _, lerr = assert_close(out[b, j], lse[b, j], ref_out, ref_lse,
+                                      what=f"{w.name} b={b} j={j}")
+            # the relative term on its own (the absolute one carries the combined
+            # tolerance where a nearly flat softmax makes |out| ~ 1e-3)
+            rel = float(np.abs(out[b, j] - ref_out).max() / np.abs(ref_out).max())
+            print(f"{w.name} {kv_dtype} b={b} j={j}: max|ref| {np.abs(ref_out).max():.3g} "
+                  f"rel err {rel:.3g} lse err {lerr:.3g}")
+            assert rel <= 1e-2, f"{w.name} b={b} j={j}: relative error {rel:.4g}"
     return out, lse, ws
 
 
