@@ -64,6 +64,12 @@ def _rank_env():
     return rank, world, local
 
 
+# Decoder layers of the served model ("How to serve trillions of tokens for
+# trillion-parameter coding agents", section "Tensor parallel was the best
+# parallelism strategy for maximum interactivity": 61 layers of 576-element
+# latent entries); one model decode step runs mla_decode once per layer.
+MODEL_LAYERS = 61
+
 FALLBACK_BF16_TFLOPS = 1900.0
 FP8_PER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 
@@ -110,21 +116,30 @@ def aggregate(values_ms, units_per_rank):
     return sum(units_per_rank) / (t / 1e3), t
 
 
-class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 50 ms."""
+def _norm_uuid(u) -> str:
+    u = str(u).strip().lower()
+    return u[4:] if u.startswith("gpu-") else u
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons of this process's GPU, every 50 ms.
+
+    Every visible GPU is sampled and the rows of the one whose UUID matches
+    ``gpu_uuid`` are kept (all rows when there is no match and only one GPU
+    answers), so that neither a UUID format nor an index remapping by
+    CUDA_VISIBLE_DEVICES can leave the record empty.
+    """
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_id: str | None):
+    def __init__(self, gpu_uuid: str | None):
         self.proc = None
-        self.t0 = None
+        self.uuid = _norm_uuid(gpu_uuid) if gpu_uuid else None
         try:
             cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                    "-lms", "50"]
-            if gpu_id:
-                cmd += ["-i", gpu_id]
             self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                                          text=True)
         except Exception:
@@ -139,16 +154,26 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = []
-        for line in out.strip().splitlines():
+        return self.summarise(out, self.uuid)
+
+    @staticmethod
+    def summarise(text: str, uuid: str | None):
+        """Median SM clock, max clock and active throttle reasons of the matching rows."""
+        by_gpu = {}
+        for line in text.strip().splitlines():
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                row = (float(parts[1]), float(parts[2]), parts[5:9])
             except ValueError:
                 continue
-        if not rows:
+            by_gpu.setdefault(_norm_uuid(parts[0]), []).append(row)
+        if uuid and uuid in by_gpu:
+            rows = by_gpu[uuid]
+        elif len(by_gpu) == 1:
+            rows = next(iter(by_gpu.values()))
+        else:
             return None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({n for _, _, flags in rows for n, f in zip(names, flags)
@@ -301,7 +326,13 @@ def run_gpu(args):
     binding.load_library()
 
     make, kv_dtype, desc = CONFIGS[args.config]
-    w = make()
+    if args.seq_len:
+        if args.config != "long":
+            raise SystemExit("--seq-len applies to the long-context workload only")
+        w = wl.long_context(seq_len=args.seq_len)
+        desc = desc.replace("L=100000", f"L={args.seq_len}")
+    else:
+        w = make()
     B, Q, H = w.batch, w.num_queries, w.num_heads
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", L2_BYTES_FALLBACK)
     bpt = accounting.kv_bytes_per_token(kv_dtype)
@@ -366,12 +397,11 @@ def run_gpu(args):
         graphs.append(g)
     torch.cuda.synchronize()
 
-    gpu_id = None
     try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
-        gpu_id = str(local)
-    sampler = ClockSampler(gpu_id)
+        gpu_uuid = None
+    sampler = ClockSampler(gpu_uuid)
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
             graphs[i % copies].replay()
@@ -391,8 +421,18 @@ def run_gpu(args):
         dist.barrier()
     clocks = sampler.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
-    decode_ms = [a.elapsed_time(b) for a, b in evs]
+    # The decode call's own duration: the events captured around it in each graph
+    # hold that graph's latest replay, so replay the graphs in rotation and read
+    # every pair after each full rotation.
+    decode_ms = []
+    with torch.cuda.stream(stream):
+        while len(decode_ms) < args.call_samples:
+            for r in range(copies):
+                graphs[r].replay()
+            stream.synchronize()
+            decode_ms += [a.elapsed_time(b) for a, b in evs]
     decode_us = 1e3 * sum(decode_ms) / len(decode_ms)
+    decode_us_median = 1e3 * statistics.median(decode_ms)
 
     elapsed_ms = slowest_rank_ms(elapsed_ms, dist)
 
@@ -504,7 +544,11 @@ def run_gpu(args):
             c1.record()
         torch.cuda.synchronize()
         check_us = 1e3 * c0.elapsed_time(c1) / (reps * per_graph)
+        # The check guards one decode step of the model, which runs mla_decode once
+        # per layer; the pages' model has 61 layers.
         kv_check = {"us_per_call": check_us, "fraction_of_decode_call": check_us / decode_us,
+                    "model_layers": MODEL_LAYERS,
+                    "fraction_of_model_step": check_us / (MODEL_LAYERS * decode_us),
                     "requests_failed": int((chk_status != 0).sum().item()),
                     "pages_checked": int(sum(-(-int(n) // 64) for n in w.seq_lens))}
 
@@ -547,8 +591,10 @@ def run_gpu(args):
             "logical_kv_gbs": world * accounting.step_bytes(w.seq_lens, Q, H, kv_dtype)["kv"]
             * steps_per_s / 1e9,
             "cpu_baseline": cpu, "e2e": e2e, "kv_check": kv_check,
-            # per step: KV append, decode and combine
-            "gpu_launches": 3 * args.steps, "clocks": clocks,
+            # per step: KV append, then mla_decode's query split, decode and combine
+            "gpu_launches": 4 * args.steps, "clocks": clocks,
+            "decode_call_us": {"mean": decode_us, "median": decode_us_median,
+                               "samples": len(decode_ms)},
             "device_status": status,
         }
         print(json.dumps(line), flush=True)
@@ -574,6 +620,10 @@ def main(argv=None):
     ap.add_argument("--no-check", action="store_true",
                     help="skip timing the integrity check (mla_kv_check) beside the decode")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--call-samples", type=int, default=400,
+                    help="event-timed decode calls behind the roofline's avg_launch_us")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="cached tokens of the long-context workload (0 = 100,000)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -26,6 +26,7 @@ MLA_KV_BF16 = 1
 
 MLA_DEVICE_ERR_BAD_PAGE = 0x1
 MLA_DEVICE_ERR_BAD_LENGTH = 0x2
+MLA_DEVICE_ERR_TIMEOUT = 0x4
 
 MLA_KV_CHECK_TAG_MISMATCH = 0x1
 MLA_KV_CHECK_PAGE_RANGE = 0x2
@@ -49,6 +50,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
+    _lib = open_library(path)
+    return _lib
+
+
+def open_library(path: str) -> ctypes.CDLL:
+    """Open a build of the library at ``path`` (not cached) with its argument types."""
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is not built; run paged_mla_decode_gb300.build.build() "
                            "(or __graft_entry__.build()) first")
@@ -82,7 +89,6 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         c.c_void_p, c.c_void_p, c.c_int64, c.c_int, c.c_int, c.c_void_p, c.c_int, c.c_void_p,
         c.c_int, c.c_int, c.c_int, c.c_float, c.c_float, c.c_int, c.c_void_p, c.c_void_p,
         c.c_void_p, c.c_void_p]
-    _lib = lib
     return lib
 
 

@@ -117,3 +117,26 @@ def test_reference_arm_line_has_the_contract_keys(capsys, monkeypatch):
     assert line["e2e"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+
+
+def test_clock_record_keeps_this_gpus_rows():
+    """The clock sampler keeps the rows of the GPU whose UUID torch reports.
+
+    nvidia-smi prints UUIDs as GPU-<uuid>; torch may give the bare UUID: both
+    spellings select the same rows, and a lone GPU is kept even without a match.
+    """
+    text = "\n".join([
+        "GPU-aaaa-1, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "GPU-bbbb-2, 1200, 2070, 300.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "GPU-aaaa-1, 2050, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "GPU-aaaa-1, 2070, 2070, 980.0, 0x4, Not Active, Not Active, Not Active, Active",
+    ])
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = bench.ClockSampler.summarise(text, "aaaa-1")
+    assert rec["samples"] == 3 and rec["sm_mhz"] == 2070 and rec["sm_max_mhz"] == 2070
+    assert rec["reasons"] == ["sw_power_cap"]
+    assert bench.ClockSampler.summarise(text, bench._norm_uuid("GPU-AAAA-1")) == rec
+    lone = "\n".join(l for l in text.splitlines() if "bbbb" in l)
+    assert bench.ClockSampler.summarise(lone, "cccc")["sm_mhz"] == 1200
+    assert bench.ClockSampler.summarise(text, "cccc") is None
