@@ -371,12 +371,28 @@ def run_gpu(args):
     ws = torch.zeros(binding.mla_decode_workspace_size(B, Q, H), dtype=torch.uint8, device=dev)
     f16_ops = args.operands == "f16"
 
+    # Forked sessions (the prefix-shared workload) go through the grouped decode,
+    # which reads each shared page once for its group, unless --plain-decode.
+    grouped = bool(w.extra.get("forks")) and not args.plain_decode and not f16_ops
+    if grouped:
+        forks = int(w.extra["forks"])
+        prefix_pages = torch.from_numpy(w.extra["prefix_pages"]).to(dev)
+        ws = torch.zeros(binding.mla_decode_grouped_workspace_size(B, Q, H), dtype=torch.uint8,
+                         device=dev)
+
+    def decode_call(qq, table, lens, o, l):
+        if grouped:
+            binding.mla_decode_grouped(qq, pages, table, lens, forks, prefix_pages, w.sm_scale,
+                                       kv_scale, o, l, ws)
+        else:
+            binding.mla_decode(qq, pages, table, lens, w.sm_scale, kv_scale, o, l, ws,
+                               f16_operands=f16_ops)
+
     def step(r, ev=None):
         binding.mla_kv_append(fresh_lat, fresh_rope, fresh_slots[r], pages, kv_scale)
         if ev is not None:
             ev[0].record()
-        binding.mla_decode(q, pages, tables_d[r], seq_lens, w.sm_scale, kv_scale, out, lse, ws,
-                           f16_operands=f16_ops)
+        decode_call(q, tables_d[r], seq_lens, out, lse)
         if ev is not None:
             ev[1].record()
 
@@ -481,8 +497,7 @@ def run_gpu(args):
         def issue(r):
             d_in.copy_(h_in[r], non_blocking=True)
             binding.mla_kv_append(d_lat, d_rope, d_slots, pages, kv_scale)
-            binding.mla_decode(d_q, pages, d_table, d_lens, w.sm_scale, kv_scale, e_out, e_lse,
-                               ws, f16_operands=f16_ops)
+            decode_call(d_q, d_table, d_lens, e_out, e_lse)
             h_res.copy_(d_res, non_blocking=True)
 
         with torch.cuda.stream(stream):
@@ -579,6 +594,8 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": kv_dtype, "data": "synthetic",
             "config": {"workload": desc, "batch": B, "queries": Q, "heads": H,
                        "mma_operands": "bf16" if kv_dtype == "bf16" else args.operands,
+                       "decode": "mla_decode_grouped" if grouped else
+                                 ("mla_decode_f16_operands" if f16_ops else "mla_decode"),
                        "seq_lens_total": int(w.seq_lens.sum()), "unique_tokens": w.unique_tokens,
                        "kv_dtype": kv_dtype, "page_size": 64,
                        "l2": f"rotating {copies} cache copies "
@@ -622,6 +639,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--call-samples", type=int, default=400,
                     help="event-timed decode calls behind the roofline's avg_launch_us")
+    ap.add_argument("--plain-decode", action="store_true",
+                    help="decode forked sessions with mla_decode instead of mla_decode_grouped")
     ap.add_argument("--seq-len", type=int, default=0,
                     help="cached tokens of the long-context workload (0 = 100,000)")
     args = ap.parse_args(argv)

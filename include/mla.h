@@ -185,6 +185,42 @@ MLA_API mla_status mla_decode(const void* q, const void* kv_pages, int64_t num_p
                       size_t workspace_bytes, void* out, float* lse, mla_stream_t stream);
 
 /*
+ * mla_decode_grouped -- mla_decode for groups of requests that share a prefix.
+ *
+ * Subagent sessions fork from a parent context ("vLLM x AgentX: Optimizing for
+ * Real-World Agentic Serving", section "Characterizing agentic workloads: a
+ * second look") and then read the pages of one physical paged cache ("Smaller,
+ * faster, safer: running Kimi and GLM at scale", section "Protecting a shared KV
+ * cache"). Requests [g * forks, (g + 1) * forks) form group g, and their first
+ * prefix_pages[g] logical pages are the same physical pages; the kernel reads
+ * those page ids from the group's first request. The results are mla_decode's
+ * on the same arguments (same arithmetic and tolerance); what changes is how
+ * the work is cut: each shared page is worked by `forks` CTAs at once, one per
+ * fork, so the group reads it from HBM once (the other forks' reads hit L2),
+ * while the tokens after the prefix are split as in mla_decode.
+ *
+ * forks         requests per group; 1 <= forks <= CTAs and batch % forks == 0
+ * prefix_pages  device, int32 [batch / forks]. A request whose group prefix is
+ *               outside [0, max_pages] pages or longer than L - num_queries + 1
+ *               tokens (draft 0 must see the whole prefix) is treated like a
+ *               bad length: out = 0, lse = -inf, MLA_DEVICE_ERR_BAD_LENGTH.
+ * workspace     at least mla_decode_grouped_workspace_size(batch, num_queries,
+ *               num_heads, num_ctas) bytes, zero-filled before its first use.
+ * kv_dtype      MLA_KV_E4M3 (MLA_ERR_UNSUPPORTED otherwise).
+ * Other arguments as mla_decode.
+ */
+MLA_API size_t mla_decode_grouped_workspace_size(int batch, int num_queries, int num_heads,
+                                                 int num_ctas);
+MLA_API mla_status mla_decode_grouped(const void* q, const void* kv_pages, int64_t num_pages,
+                                      int page_size, int kv_dtype, const int32_t* block_table,
+                                      int max_pages, const int32_t* seq_lens, int batch,
+                                      int num_queries, int num_heads, int forks,
+                                      const int32_t* prefix_pages, float sm_scale,
+                                      float kv_scale, int num_ctas, void* workspace,
+                                      size_t workspace_bytes, void* out, float* lse,
+                                      mla_stream_t stream);
+
+/*
  * mla_decode_f16_operands -- mla_decode with 16-bit tensor-core operands.
  *
  * Same arguments, contract and results (within the same tolerance) as

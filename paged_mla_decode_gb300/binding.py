@@ -34,6 +34,7 @@ MLA_KV_CHECK_BAD_LENGTH = 0x4
 
 EXPORTED = ("mla_abi_version", "mla_status_string", "mla_kv_append",
             "mla_decode_workspace_size", "mla_decode", "mla_decode_f16_operands",
+            "mla_decode_grouped_workspace_size", "mla_decode_grouped",
             "mla_decode_combine", "mla_kv_check", "mla_decode_static_scratch")
 
 _lib = None
@@ -77,6 +78,14 @@ def open_library(path: str) -> ctypes.CDLL:
                                c.c_void_p, c.c_void_p]
     lib.mla_decode_f16_operands.restype = c.c_int
     lib.mla_decode_f16_operands.argtypes = lib.mla_decode.argtypes
+    lib.mla_decode_grouped_workspace_size.restype = c.c_size_t
+    lib.mla_decode_grouped_workspace_size.argtypes = [c.c_int, c.c_int, c.c_int, c.c_int]
+    lib.mla_decode_grouped.restype = c.c_int
+    lib.mla_decode_grouped.argtypes = [c.c_void_p, c.c_void_p, c.c_int64, c.c_int, c.c_int,
+                                       c.c_void_p, c.c_int, c.c_void_p, c.c_int, c.c_int,
+                                       c.c_int, c.c_int, c.c_void_p, c.c_float, c.c_float,
+                                       c.c_int, c.c_void_p, c.c_size_t, c.c_void_p, c.c_void_p,
+                                       c.c_void_p]
     lib.mla_decode_combine.restype = c.c_int
     lib.mla_decode_combine.argtypes = [c.c_void_p, c.c_void_p, c.c_int, c.c_int64, c.c_void_p,
                                        c.c_void_p, c.c_void_p]
@@ -165,6 +174,35 @@ def mla_decode(q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tenso
         int(workspace.numel() * workspace.element_size()), _ptr(out), _ptr(lse),
         _stream(stream))
     _check(st, "mla_decode_f16_operands" if f16_operands else "mla_decode")
+
+
+def mla_decode_grouped_workspace_size(batch: int, num_queries: int, num_heads: int,
+                                      num_ctas: int = 0) -> int:
+    return int(load_library().mla_decode_grouped_workspace_size(batch, num_queries, num_heads,
+                                                                num_ctas))
+
+
+def mla_decode_grouped(q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tensor,
+                       seq_lens: torch.Tensor, forks: int, prefix_pages: torch.Tensor,
+                       sm_scale: float, kv_scale: float, out: torch.Tensor, lse: torch.Tensor,
+                       workspace: torch.Tensor, num_ctas: int = 0, stream=None) -> None:
+    """mla_decode for groups of ``forks`` requests sharing ``prefix_pages[g]`` pages."""
+    assert q.dtype == torch.bfloat16 and q.dim() == 4 and q.shape[3] == 576 and q.is_contiguous()
+    batch, nq, heads, _ = q.shape
+    assert block_table.dtype == torch.int32 and block_table.dim() == 2
+    assert block_table.is_contiguous() and block_table.shape[0] == batch
+    assert seq_lens.dtype == torch.int32 and seq_lens.numel() == batch
+    assert prefix_pages.dtype == torch.int32 and prefix_pages.is_contiguous()
+    assert out.dtype == torch.bfloat16 and tuple(out.shape) == (batch, nq, heads, 512)
+    assert lse.dtype == torch.float32 and tuple(lse.shape) == (batch, nq, heads)
+    assert kv_pages.is_contiguous() and kv_pages.dim() == 3 and kv_pages.shape[2] == 576
+    st = load_library().mla_decode_grouped(
+        _ptr(q), _ptr(kv_pages), int(kv_pages.shape[0]), int(kv_pages.shape[1]),
+        kv_dtype_code(kv_pages), _ptr(block_table), int(block_table.shape[1]), _ptr(seq_lens),
+        batch, nq, heads, int(forks), _ptr(prefix_pages), float(sm_scale), float(kv_scale),
+        int(num_ctas), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+        _ptr(out), _ptr(lse), _stream(stream))
+    _check(st, "mla_decode_grouped")
 
 
 def mla_decode_combine(part_out: torch.Tensor, part_lse: torch.Tensor, out: torch.Tensor,

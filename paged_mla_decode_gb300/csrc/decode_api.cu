@@ -24,14 +24,25 @@ namespace {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 }  // namespace
 
-extern "C" size_t mla_decode_workspace_size(int batch, int num_queries, int num_heads,
-                                            int num_ctas) {
+namespace {
+size_t workspace_bytes_for(int batch, int num_queries, int num_heads, int num_ctas, int passes) {
   if (batch < 0 || num_queries < 1 || num_queries > MLA_MAX_QUERIES || num_heads <= 0 ||
       num_ctas < 0)
     return 0;
   if (num_ctas == 0) num_ctas = mla::device_sm_count();
   if (num_ctas <= 0) return 0;
-  return mla::workspace_layout((int64_t)batch * num_queries, num_heads, num_ctas).total;
+  return mla::workspace_layout((int64_t)batch * num_queries, num_heads, num_ctas, passes).total;
+}
+}  // namespace
+
+extern "C" size_t mla_decode_workspace_size(int batch, int num_queries, int num_heads,
+                                            int num_ctas) {
+  return workspace_bytes_for(batch, num_queries, num_heads, num_ctas, 1);
+}
+
+extern "C" size_t mla_decode_grouped_workspace_size(int batch, int num_queries, int num_heads,
+                                                    int num_ctas) {
+  return workspace_bytes_for(batch, num_queries, num_heads, num_ctas, 2);
 }
 
 namespace {
@@ -40,7 +51,7 @@ mla_status decode_impl(const void* q, const void* kv_pages, int64_t num_pages, i
                        const int32_t* seq_lens, int batch, int num_queries, int num_heads,
                        float sm_scale, float kv_scale, int num_ctas, void* workspace,
                        size_t workspace_bytes, void* out, float* lse, mla_stream_t stream,
-                       bool f16_operands) {
+                       bool f16_operands, int forks = 1, const int32_t* prefix_pages = nullptr) {
   using namespace mla;
   if (batch < 0 || num_pages < 0 || max_pages < 1 || num_ctas < 0) return MLA_ERR_INVALID_ARG;
   if (num_queries < 1 || num_queries > MLA_MAX_QUERIES) return MLA_ERR_INVALID_ARG;
@@ -59,7 +70,10 @@ mla_status decode_impl(const void* q, const void* kv_pages, int64_t num_pages, i
   if (G <= 0) return MLA_ERR_CUDA;
   const int64_t rows = (int64_t)batch * num_queries;
   if (rows * num_heads > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
-  const WorkspaceLayout L = workspace_layout(rows, num_heads, G);
+  const bool grouped = prefix_pages != nullptr;
+  if (grouped && (forks < 1 || forks > G || batch % forks != 0)) return MLA_ERR_INVALID_ARG;
+  if (grouped && !aligned(prefix_pages, 4)) return MLA_ERR_INVALID_ARG;
+  const WorkspaceLayout L = workspace_layout(rows, num_heads, G, grouped ? 2 : 1);
   if (workspace_bytes < L.total) return MLA_ERR_WORKSPACE;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -80,6 +94,7 @@ mla_status decode_impl(const void* q, const void* kv_pages, int64_t num_pages, i
   p.ws.status = reinterpret_cast<unsigned*>(ws);
   p.ws.row_base = reinterpret_cast<int32_t*>(ws + L.row_base);
   p.ws.row_np = reinterpret_cast<int32_t*>(ws + L.row_np);
+  p.ws.row_np1 = reinterpret_cast<int32_t*>(ws + L.row_np1);
   p.ws.piece_err = reinterpret_cast<int32_t*>(ws + L.piece_err);
   p.ws.part_lse = reinterpret_cast<float*>(ws + L.part_lse);
   p.ws.part_out = reinterpret_cast<float*>(ws + L.part_out);
@@ -87,6 +102,11 @@ mla_status decode_impl(const void* q, const void* kv_pages, int64_t num_pages, i
   p.ws.q_mul = reinterpret_cast<float*>(ws + L.q_mul);
 
   if (!p.bf16 && num_pages > (int64_t)(0x7fffffff / kPageSize)) return MLA_ERR_UNSUPPORTED;
+  if (grouped) {
+    if (p.bf16 || f16_operands) return MLA_ERR_UNSUPPORTED;  // FP8 cache, FP8 operands only
+    p.forks = forks;
+    p.prefix_pages = prefix_pages;
+  }
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = (p.bf16 || f16_operands) ? launch_decode_tensor_core(p, s)
@@ -120,4 +140,18 @@ extern "C" mla_status mla_decode_f16_operands(const void* q, const void* kv_page
   return decode_impl(q, kv_pages, num_pages, page_size, kv_dtype, block_table, max_pages,
                      seq_lens, batch, num_queries, num_heads, sm_scale, kv_scale, num_ctas,
                      workspace, workspace_bytes, out, lse, stream, true);
+}
+
+extern "C" mla_status mla_decode_grouped(const void* q, const void* kv_pages, int64_t num_pages,
+                                         int page_size, int kv_dtype, const int32_t* block_table,
+                                         int max_pages, const int32_t* seq_lens, int batch,
+                                         int num_queries, int num_heads, int forks,
+                                         const int32_t* prefix_pages, float sm_scale,
+                                         float kv_scale, int num_ctas, void* workspace,
+                                         size_t workspace_bytes, void* out, float* lse,
+                                         mla_stream_t stream) {
+  if (batch > 0 && prefix_pages == nullptr) return MLA_ERR_INVALID_ARG;
+  return decode_impl(q, kv_pages, num_pages, page_size, kv_dtype, block_table, max_pages,
+                     seq_lens, batch, num_queries, num_heads, sm_scale, kv_scale, num_ctas,
+                     workspace, workspace_bytes, out, lse, stream, false, forks, prefix_pages);
 }

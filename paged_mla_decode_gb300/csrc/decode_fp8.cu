@@ -41,6 +41,7 @@
 // Every wait is bounded (2 s); on timeout the CTA records MLA_DEVICE_ERR_TIMEOUT,
 // stops, drains its MMAs and copies (bounded, 2 s) and frees TMEM.
 #include <atomic>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -122,6 +123,9 @@ constexpr int kNumBars = 2 * kRing + 15 + kPBufs;
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024 alignment
+// grouped decode: the two segments' plans (int64 [32]) after the common map
+constexpr int kOffPlanX = (kSmemUsed + 15) & ~15;
+constexpr int kSmemBytesGrouped = kOffPlanX + 256 + 1024;
 
 enum Flag { F_ABORT = 0, F_PIECE_BAD = 1 };
 
@@ -136,6 +140,7 @@ struct PageDesc {
   int32_t slot;    // partial slot of this piece
 };
 constexpr int16_t kDescPieceStart = 1, kDescPieceEnd = 2, kDescPageOk = 4;
+constexpr int16_t kDescShared = 8;  // grouped decode: a shared-prefix page (informational)
 
 struct Fp8Params {
   const __nv_bfloat16* q;
@@ -149,26 +154,52 @@ struct Fp8Params {
   float kv_scale;
   int G;
   DecodeWorkspace ws;
+  // grouped decode (decode_fp8_kernel<true>) only
+  int forks;                    // requests per group
+  int workers;                  // CTAs / forks: workers of the shared-prefix plan
+  const int32_t* prefix_pages;  // [batch / forks] shared pages of each group
 };
+
+__device__ inline GroupPlan group_plan(const Fp8Params& p, int kind) {
+  return GroupPlan{p.seq_lens, p.batch, p.nq, p.max_pages, kPageSize,
+                   kind == 1 ? p.workers : p.G, 0, kind, p.forks, p.prefix_pages};
+}
 
 // Cursor over a CTA's pages (one page per step). The row's partial slot and
 // block-table offset are computed once per row: a step costs no division.
+// `cta` is the worker index in the plan; for the grouped decode's plans the
+// slot comes from the row table and `fork` picks the query row.
+template <class P>
 struct PageWalker {
-  Plan plan;
+  P plan;
   RowCursor cur;
   int64_t x, x_end, x_begin;
-  int cta;         // this CTA's index
+  int cta;         // this CTA's worker index in the plan
+  int fork;        // grouped decode: the fork this CTA works for
   int slot;        // partial slot of the current row's piece in this CTA
-  int64_t bt_row;  // block-table offset of the current row's request
+  int qrow;        // query / output row of the current row
+  int64_t bt_row;  // block-table offset of the current row's first page
+  const int32_t* row_base;  // grouped decode: the row table
+  const int32_t* row_np1;
 
-  __device__ void init(const Plan& p, const RowCursor& c, int cta_index, int64_t xb, int64_t xe) {
+  __device__ void init(const P& p, const RowCursor& c, int cta_index, int64_t xb, int64_t xe,
+                       int fork_index = 0, const int32_t* rb = nullptr,
+                       const int32_t* np1 = nullptr) {
     plan = p; cur = c; cta = cta_index; x = xb; x_begin = xb; x_end = xe;
+    fork = fork_index; row_base = rb; row_np1 = np1;
     row_changed();
     settle();
   }
   __device__ void row_changed() {
-    slot = cur.base + (cta - plan.cta_of(cur.rt));
-    bt_row = (int64_t)(cur.r / plan.nq) * plan.max_pages;
+    if constexpr (P::kGrouped) {
+      qrow = plan.q_row(cur.r, fork);
+      slot = __ldcg(row_base + qrow) + (plan.kind == 2 ? __ldcg(row_np1 + qrow) : 0) +
+             (cta - plan.cta_of(cur.rt));
+    } else {
+      qrow = cur.r;
+      slot = cur.base + (cta - plan.cta_of(cur.rt));
+    }
+    bt_row = plan.bt_base(cur.r);
   }
   __device__ void settle() {
     if (x < x_end && x == cur.rt + cur.t) {
@@ -181,6 +212,34 @@ struct PageWalker {
   __device__ bool piece_end() const { return x + 1 == x_end || x + 1 == cur.rt + cur.t; }
   __device__ int valid_tokens() const { return min(kPageSize, cur.n - page_in_row() * kPageSize); }
   __device__ void next() { ++x; settle(); }
+  __device__ bool shared() const { return false; }
+};
+
+// The grouped decode's walker: this CTA's range of the shared-prefix plan (as
+// fork `fork` of its worker), then its range of the suffix plan.
+struct SegWalker : PageWalker<GroupPlan> {
+  GroupPlan B;
+  RowCursor curB;
+  int64_t xbB, xeB;
+  int ctaB;
+  bool in_prefix;
+  __device__ void start(const GroupPlan& A, const RowCursor& ca, int64_t xbA, int64_t xeA,
+                        int worker, int fork_index, const GroupPlan& Bp, const RowCursor& cb,
+                        int64_t xb, int64_t xe, int cta_index, const int32_t* rb,
+                        const int32_t* np1) {
+    B = Bp; curB = cb; xbB = xb; xeB = xe; ctaB = cta_index;
+    in_prefix = xbA < xeA;
+    if (in_prefix) init(A, ca, worker, xbA, xeA, fork_index, rb, np1);
+    else init(B, curB, ctaB, xbB, xeB, 0, rb, np1);
+  }
+  __device__ void next() {
+    PageWalker<GroupPlan>::next();
+    if (in_prefix && x == x_end) {
+      in_prefix = false;
+      if (xbB < xeB) init(B, curB, ctaB, xbB, xeB, 0, row_base, row_np1);
+    }
+  }
+  __device__ bool shared() const { return in_prefix; }
 };
 
 __device__ __forceinline__ void named_bar_softmax() {
@@ -214,6 +273,9 @@ __device__ __forceinline__ uint32_t e5m2x2_of(float lo, float hi) {
   return r;
 }
 
+// kGrouped: the grouped decode (GroupPlan): this CTA's shared-prefix range, then
+// its suffix range; otherwise mla_decode's single plan (Plan).
+template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fp8_kernel(const Fp8Params p, const __grid_constant__ CUtensorMap lat_map,
                       const __grid_constant__ CUtensorMap rope_map) {
@@ -241,19 +303,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   Plan plan{p.seq_lens, p.batch, p.nq, p.max_pages, kPageSize, p.G, 0};
   const int c = blockIdx.x;
+  int64_t* s_plan_x = reinterpret_cast<int64_t*>(smem + kOffPlanX);  // kGrouped only
   if (warp == 0) {
-    // the whole plan in one warp pass: total tiles, then this CTA's first row
-    Plan pl = plan;
-    pl.set_total(plan_total_tiles_warp(pl));
-    const int64_t xb = c < pl.G ? pl.cta_start(c) : 0;
-    RowCursor f = plan_find_row_warp(pl, xb, c == 0, p.ws.row_base, p.ws.row_np, p.ws.status);
-    if (lane == 0) {
-      s_plan[0] = pl.T;
-      s_plan[1] = f.r;
-      s_plan[2] = f.rt;
-      s_plan[3] = f.t;
-      s_plan[4] = f.base;
-      s_plan[5] = f.n;
+    if constexpr (kGrouped) {
+      // both plans (row table written by group_plan_kernel): this CTA's prefix
+      // range as fork f of worker w, then its suffix range
+      GroupPlan A = group_plan(p, 1), B = group_plan(p, 2);
+      A.set_total(plan_total_tiles_warp(A));
+      B.set_total(plan_total_tiles_warp(B));
+      const int w = c / p.forks, f = c - w * p.forks;
+      const bool in_a = c < p.forks * p.workers && w < A.G;
+      const bool in_b = c < B.G;
+      const int64_t xba = in_a ? A.cta_start(w) : 0, xea = in_a ? A.cta_start(w + 1) : 0;
+      const int64_t xbb = in_b ? B.cta_start(c) : 0, xeb = in_b ? B.cta_start(c + 1) : 0;
+      RowCursor fa{0, 0, 0, 0, 0}, fb{0, 0, 0, 0, 0};
+      if (in_a) fa = plan_find_row_warp(A, xba, false, p.ws.row_base, p.ws.row_np, p.ws.status);
+      if (in_b) fb = plan_find_row_warp(B, xbb, false, p.ws.row_base, p.ws.row_np, p.ws.status);
+      if (lane == 0) {
+        s_plan[0] = (xea - xba) + (xeb - xbb);                 // pages of this CTA
+        s_plan[1] = xea > xba ? A.q_row(fa.r, f) : fb.r;       // query row of its first piece
+        const int64_t v[20] = {A.T, B.T, xba, xea, xbb, xeb, w, f, fa.r, fa.rt, fa.t, fa.base,
+                               fa.n, fb.r, fb.rt, fb.t, fb.base, fb.n, 0, 0};
+        for (int i = 0; i < 20; ++i) s_plan_x[i] = v[i];
+      }
+    } else {
+      // the whole plan in one warp pass: total tiles, then this CTA's first row
+      Plan pl = plan;
+      pl.set_total(plan_total_tiles_warp(pl));
+      const int64_t xb = c < pl.G ? pl.cta_start(c) : 0;
+      RowCursor f = plan_find_row_warp(pl, xb, c == 0, p.ws.row_base, p.ws.row_np, p.ws.status);
+      if (lane == 0) {
+        s_plan[0] = pl.T;
+        s_plan[1] = f.r;
+        s_plan[2] = f.rt;
+        s_plan[3] = f.t;
+        s_plan[4] = f.base;
+        s_plan[5] = f.n;
+      }
     }
   }
   if (warp == kPvWarp && lane == 0) {
@@ -275,10 +361,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   griddep_launch_dependents();  // the combine kernel may be scheduled (it waits for this grid)
-  plan.set_total(s_plan[0]);
-  const bool works = c < plan.G;
-  const int64_t x_begin = works ? plan.cta_start(c) : 0;
-  const int64_t x_end = works ? plan.cta_start(c + 1) : 0;
+  int64_t x_begin = 0, x_end = 0;
+  if constexpr (kGrouped) {
+    x_end = s_plan[0];
+  } else {
+    plan.set_total(s_plan[0]);
+    const bool works = c < plan.G;
+    x_begin = works ? plan.cta_start(c) : 0;
+    x_end = works ? plan.cta_start(c + 1) : 0;
+  }
   const uint32_t tmem = *tmem_slot;
   const RowCursor cur0{(int)s_plan[1], s_plan[2], (int)s_plan[3], (int)s_plan[4],
                        (int)s_plan[5]};
@@ -301,20 +392,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const uint64_t pol = l2_evict_first_policy();
         PageDesc* ring = reinterpret_cast<PageDesc*>(smem + kOffDesc);
-        PageWalker pw;
-        pw.init(plan, cur0, c, x_begin, x_end);
+        std::conditional_t<kGrouped, SegWalker, PageWalker<Plan>> pw;
+        if constexpr (kGrouped) {
+          GroupPlan A = group_plan(p, 1), B = group_plan(p, 2);
+          A.set_total(s_plan_x[0]);
+          B.set_total(s_plan_x[1]);
+          const RowCursor ca{(int)s_plan_x[8], s_plan_x[9], (int)s_plan_x[10],
+                             (int)s_plan_x[11], (int)s_plan_x[12]};
+          const RowCursor cb{(int)s_plan_x[13], s_plan_x[14], (int)s_plan_x[15],
+                             (int)s_plan_x[16], (int)s_plan_x[17]};
+          pw.start(A, ca, s_plan_x[2], s_plan_x[3], (int)s_plan_x[6], (int)s_plan_x[7], B, cb,
+                   s_plan_x[4], s_plan_x[5], c, p.ws.row_base, p.ws.row_np1);
+        } else {
+          pw.init(plan, cur0, c, x_begin, x_end);
+        }
         int64_t jn = 0;  // next page to describe
         auto describe_next = [&]() {
           PageDesc& d = ring[jn % kDescRing];
           const bool ps = pw.piece_start();
           d.valid = (int16_t)pw.valid_tokens();
-          d.flags = (int16_t)((ps ? kDescPieceStart : 0) | (pw.piece_end() ? kDescPieceEnd : 0));
-          d.row = pw.cur.r;
+          d.flags = (int16_t)((ps ? kDescPieceStart : 0) | (pw.piece_end() ? kDescPieceEnd : 0) |
+                              (pw.shared() ? kDescShared : 0));
+          d.row = pw.qrow;
           d.slot = pw.slot;
           cp_async_4(smem_u32(&d.page), p.block_table + pw.bt_row + pw.page_in_row());
           cp_async_commit();
           if (ps && jn > 0)  // the softmax warps read this row's q when they reach it
-            tc::prefetch_l2_bulk(p.q + (int64_t)pw.cur.r * H * kDEntry,
+            tc::prefetch_l2_bulk(p.q + (int64_t)pw.qrow * H * kDEntry,
                                  (uint32_t)(H * kDEntry * sizeof(__nv_bfloat16)));
           pw.next();
           ++jn;
@@ -343,6 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (page_ok) {
             tc::mbar_arrive_expect_tx(bar(BAR_PAGE_FULL + slot), (uint32_t)kPageBytes);
             const int y = page * kPageSize;
+            // (a grouped decode's shared page is read by the other forks' CTAs a
+            // few pages' time later, well within the life of an evict-first line)
 #pragma unroll
             for (int b = 0; b < 4; ++b)
               tc::tma_load_2d_hint(page_base + b * kLatBlock, &lat_map, 128 * b, y,
@@ -833,6 +939,69 @@ __global__ void __launch_bounds__(kSplitThreads)
   if (u == 0) q_mul[row * 64 + h] = score_mul * ldexpf(1.0f, -shift);
 }
 
+// ---- grouped decode: the row table of both plans (one warp) ----
+// For every (request, draft) row r: row_np1[r] = its shared-prefix pieces (those
+// of its group's prefix row, one per worker that the prefix row spans), row_np[r]
+// = row_np1[r] + its suffix pieces (-1 for a bad row, which still owns its
+// row_np1[r] prefix slots), row_base[r] = the sum of the earlier rows' slots.
+__global__ void __launch_bounds__(32) group_plan_kernel(const Fp8Params p) {
+  griddep_wait();  // all earlier work in the stream is complete
+  griddep_launch_dependents();
+  const int lane = threadIdx.x;
+  GroupPlan A = group_plan(p, 1), B = group_plan(p, 2);
+  A.set_total(plan_total_tiles_warp(A));
+  B.set_total(plan_total_tiles_warp(B));
+  int64_t rt_carry = 0;
+  for (int v0 = 0; v0 < A.rows(); v0 += 32) {
+    const int v = v0 + lane;
+    const int t = v < A.rows() ? A.row_tiles(v) : 0;
+    int64_t incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    const int64_t rt = rt_carry + incl - t;
+    if (v < A.rows()) {
+      const int np1 = A.row_pieces(rt, t);
+      for (int f = 0; f < p.forks; ++f) p.ws.row_np1[A.q_row(v, f)] = np1;
+    }
+    rt_carry = __shfl_sync(0xffffffffu, rt_carry + incl, 31);
+  }
+  __syncwarp();
+  rt_carry = 0;
+  int base_carry = 0;
+  for (int r0 = 0; r0 < B.rows(); r0 += 32) {
+    const int r = r0 + lane;
+    const bool live = r < B.rows();
+    const int t = live ? B.row_tiles(r) : 0;
+    int64_t incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    const int64_t rt = rt_carry + incl - t;
+    // a bad row keeps the slots of its prefix pieces (the prefix pass writes them
+    // for every fork of a valid group prefix) but is empty for the merge
+    const bool bad = live && B.row_tokens(r) < 0;
+    const int np = live ? p.ws.row_np1[r] + B.row_pieces(rt, t) : 0;
+    int incl_np = np;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl_np, o);
+      if (lane >= o) incl_np += u;
+    }
+    if (live) {
+      p.ws.row_base[r] = base_carry + incl_np - np;
+      p.ws.row_np[r] = bad ? -1 : np;
+      if (bad) atomicOr(p.ws.status, MLA_DEVICE_ERR_BAD_LENGTH);
+    }
+    rt_carry = __shfl_sync(0xffffffffu, rt_carry + incl, 31);
+    base_carry = __shfl_sync(0xffffffffu, base_carry + incl_np, 31);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
@@ -840,11 +1009,15 @@ cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !configured[dev].load()) {
-    cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel,
+    cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_fp8_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytesGrouped);
     if (e != cudaSuccess) return e;
     configured[dev].store(1);
   }
+  const bool grouped = d.prefix_pages != nullptr;
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (encode == nullptr) {
     cudaDriverEntryPointQueryResult qr;
@@ -885,7 +1058,20 @@ cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
   p.kv_scale = d.kv_scale;
   p.G = d.G;
   p.ws = d.ws;
+  p.forks = grouped ? d.forks : 1;
+  p.workers = grouped ? d.G / d.forks : 0;
+  p.prefix_pages = d.prefix_pages;
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  if (grouped) {
+    cudaLaunchConfig_t gc = {};
+    gc.gridDim = dim3(1);
+    gc.blockDim = dim3(32);
+    gc.stream = stream;
+    gc.attrs = attr;
+    gc.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&gc, group_plan_kernel, p);
+    if (e != cudaSuccess) return e;
+  }
   {
     const int groups = (d.heads + kSplitHeads - 1) / kSplitHeads;
     cudaLaunchConfig_t sc = {};
@@ -901,11 +1087,12 @@ cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)d.G);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = grouped ? kSmemBytesGrouped : kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_fp8_kernel, p, lat_map, rope_map);
+  return grouped ? cudaLaunchKernelEx(&cfg, decode_fp8_kernel<true>, p, lat_map, rope_map)
+                 : cudaLaunchKernelEx(&cfg, decode_fp8_kernel<false>, p, lat_map, rope_map);
 }
 
 }  // namespace mla

@@ -28,6 +28,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 //   [0, 256)                 header: uint32 status word (sticky MLA_DEVICE_ERR_*)
 //   row_base  int32[R]       first partial slot of each (request, draft) row
 //   row_np    int32[R]       number of partial slots of the row; -1 = bad length
+//   row_np1   int32[R]       grouped decode: slots of the row's shared-prefix pieces
 //   piece_err int32[P]       1 if the piece met a bad page id
 //   part_lse  float[P][H]    log-sum-exp of each piece (natural log)
 //   part_out  float[P][H][512] normalised partial output of each piece
@@ -41,18 +42,22 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kQOpChunks = kDEntry / 16;               // 36 chunks of 16 dims
 constexpr int kQOpRowBytes = kQOpChunks * 128 * 16;    // 73,728 B per row
 struct WorkspaceLayout {
-  size_t row_base, row_np, piece_err, part_lse, part_out, q_op, q_mul, total;
+  size_t row_base, row_np, row_np1, piece_err, part_lse, part_out, q_op, q_mul, total;
   int64_t max_pieces;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline WorkspaceLayout workspace_layout(int64_t rows, int heads, int num_ctas) {
+// `passes` is 1 for mla_decode and 2 for the grouped decode, whose prefix and
+// suffix passes each add up to num_ctas + rows pieces.
+__host__ __device__ inline WorkspaceLayout workspace_layout(int64_t rows, int heads, int num_ctas,
+                                                            int passes = 1) {
   WorkspaceLayout w;
-  w.max_pieces = num_ctas + rows;
+  w.max_pieces = (int64_t)passes * (num_ctas + rows);
   size_t off = 256;
   w.row_base = off; off = align_up(off + 4 * rows, 256);
   w.row_np = off; off = align_up(off + 4 * rows, 256);
+  w.row_np1 = off; off = align_up(off + 4 * rows, 256);
   w.piece_err = off; off = align_up(off + 4 * w.max_pieces, 256);
   w.part_lse = off; off = align_up(off + 4 * w.max_pieces * heads, 256);
   w.part_out = off; off = align_up(off + 4 * w.max_pieces * heads * (int64_t)kDLatent, 256);
@@ -76,6 +81,7 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int64_t rows, int he
 // first and last piece each hold one piece of it.
 // ---------------------------------------------------------------------------
 struct Plan {
+  static constexpr bool kGrouped = false;
   const int32_t* seq_lens;
   int batch, nq, max_pages, tile;
   int G;          // working CTAs: min(launched CTAs, T)
@@ -105,6 +111,10 @@ struct Plan {
   __device__ int row_pieces(int64_t rt, int t) const {
     return t == 0 ? 0 : cta_of(rt + t - 1) - cta_of(rt) + 1;
   }
+  // query / output row of plan row r (for fork f), and block-table element
+  // offset of row r's first page
+  __device__ int q_row(int r, int /*fork*/) const { return r; }
+  __device__ int64_t bt_base(int r) const { return (int64_t)(r / nq) * max_pages; }
 };
 
 // Cursor over a CTA's tiles. All threads of a CTA keep identical copies.
@@ -116,7 +126,85 @@ struct RowCursor {
   int n;          // visible tokens of row r
 };
 
-__device__ inline void cursor_next_row(const Plan& p, RowCursor& cur) {
+// ---------------------------------------------------------------------------
+// Grouped decode (requests that share a prefix).
+//
+// Requests [g*F, (g+1)*F) form group g; their first prefix_pages[g] block-table
+// entries name the same physical pages (a shared context that forked into F
+// sessions). The work is two plans of the same shape as Plan:
+//   kind 1 (prefix): one row per (group, draft) over the group's prefix pages,
+//     cut over W = CTAs / F workers; CTA c works for worker c / F as fork c % F,
+//     so the F forks of a group read each shared page at the same time (from
+//     HBM once, the others from L2) and each writes its own partial;
+//   kind 2 (suffix): one row per (request, draft) over the tokens after the
+//     prefix, cut over all CTAs like Plan.
+// Partial slots come from a row table laid out by group_plan_kernel: row r's
+// slots are [row_base[r], +row_np1[r]) for its prefix pieces (ordered by
+// worker), then its suffix pieces (ordered by CTA).
+// A row is bad (no pieces, out = 0, lse = -inf) if its length is outside
+// [Q, max_pages * 64], if prefix_pages[g] is outside [0, max_pages] or if the
+// prefix is longer than L - Q + 1 (draft 0 must see all of it).
+// ---------------------------------------------------------------------------
+struct GroupPlan {
+  static constexpr bool kGrouped = true;
+  const int32_t* seq_lens;
+  int batch, nq, max_pages, tile;
+  int G;          // workers: min(workers of the launch, T)
+  int64_t T;
+  int kind;       // 1 prefix, 2 suffix
+  int forks;
+  const int32_t* prefix_pages;
+
+  __device__ void set_total(int64_t total) {
+    T = total;
+    if (T < G) G = (int)T;
+  }
+  __device__ int groups() const { return batch / forks; }
+  __device__ int rows() const { return (kind == 1 ? groups() : batch) * nq; }
+  __device__ int group_prefix(int g) const {
+    const int pp = __ldg(prefix_pages + g);
+    return (pp < 0 || pp > max_pages) ? -1 : pp;
+  }
+  // whether request b can be decoded with its group's prefix
+  __device__ bool request_ok(int b, int pp) const {
+    const int L = __ldg(seq_lens + b);
+    return pp >= 0 && L >= nq && (int64_t)L <= (int64_t)max_pages * kPageSize &&
+           (int64_t)pp * kPageSize <= (int64_t)L - nq + 1;
+  }
+  __device__ int row_tokens(int r) const {
+    const int j = r - (r / nq) * nq;
+    if (kind == 1) {
+      const int pp = group_prefix(r / nq);
+      return pp < 0 ? -1 : pp * kPageSize;
+    }
+    const int b = r / nq;
+    const int pp = group_prefix(b / forks);
+    if (!request_ok(b, pp)) return -1;
+    return __ldg(seq_lens + b) - nq + j + 1 - pp * kPageSize;
+  }
+  __device__ int row_tiles(int r) const {
+    int n = row_tokens(r);
+    return n <= 0 ? 0 : (n + tile - 1) / tile;
+  }
+  __device__ int64_t cta_start(int c) const { return (int64_t)c * T / G; }
+  __device__ int cta_of(int64_t x) const { return (int)(((x + 1) * G - 1) / T); }
+  __device__ int row_pieces(int64_t rt, int t) const {
+    return t == 0 ? 0 : cta_of(rt + t - 1) - cta_of(rt) + 1;
+  }
+  __device__ int q_row(int r, int fork) const {
+    if (kind == 2) return r;
+    const int g = r / nq, j = r - (r / nq) * nq;
+    return (g * forks + fork) * nq + j;
+  }
+  __device__ int64_t bt_base(int r) const {
+    const int b = (kind == 1) ? (r / nq) * forks : r / nq;
+    const int64_t off = (int64_t)b * max_pages;
+    return kind == 1 ? off : off + group_prefix(b / forks);
+  }
+};
+
+template <class P>
+__device__ inline void cursor_next_row(const P& p, RowCursor& cur) {
   do {
     cur.base += p.row_pieces(cur.rt, cur.t);
     cur.rt += cur.t;
@@ -127,7 +215,8 @@ __device__ inline void cursor_next_row(const Plan& p, RowCursor& cur) {
 }
 
 // Total tiles T, computed by one warp (loop over rows, shuffle reduction).
-__device__ inline int64_t plan_total_tiles_warp(const Plan& p) {
+template <class P>
+__device__ inline int64_t plan_total_tiles_warp(const P& p) {
   int lane = threadIdx.x & 31;
   int64_t acc = 0;
   for (int r = lane; r < p.rows(); r += 32) acc += p.row_tiles(r);
@@ -139,7 +228,8 @@ __device__ inline int64_t plan_total_tiles_warp(const Plan& p) {
 // Walks rows with one warp to find the row containing tile x0 and its
 // RowCursor; optionally writes the row table (row_base / row_np) for all rows.
 // Returns the cursor in lane 0's result (all lanes get the same value).
-__device__ inline RowCursor plan_find_row_warp(const Plan& p, int64_t x0, bool write_table,
+template <class P>
+__device__ inline RowCursor plan_find_row_warp(const P& p, int64_t x0, bool write_table,
                                                int32_t* row_base, int32_t* row_np,
                                                unsigned* status) {
   int lane = threadIdx.x & 31;

@@ -16,6 +16,7 @@ struct DecodeWorkspace {
   unsigned* status;
   int32_t* row_base;
   int32_t* row_np;
+  int32_t* row_np1;   // grouped decode: slots of each row's shared-prefix pieces
   int32_t* piece_err;
   float* part_lse;
   float* part_out;
@@ -37,6 +38,10 @@ struct DecodeLaunch {
   float kv_scale;
   int G;             // CTAs launched
   DecodeWorkspace ws;
+  // FP8 grouped decode only (else prefix_pages == nullptr): requests
+  // [g * forks, (g + 1) * forks) share their first prefix_pages[g] pages
+  int forks = 1;
+  const int32_t* prefix_pages = nullptr;
 };
 
 // Split-KV decode on the tcgen05 tensor cores (decode_tc.cu); heads <= 64.

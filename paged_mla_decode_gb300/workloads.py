@@ -230,21 +230,28 @@ def concurrent(seed: int = 2, batch: int = 32, lo: int = 60_000, hi: int = 140_0
 
 def prefix_shared(seed: int = 3, groups: int = 16, forks: int = 4, prefix: int = 120_000,
                   suffix_median: float = 2000.0, suffix_sigma: float = 1.0,
-                  suffix_max: int = 20_000) -> Workload:
-    """16 groups x 4 forks; each group shares one physical 120k-token prefix."""
+                  suffix_max: int = 20_000, num_queries: int = 1,
+                  num_heads: int = 64) -> Workload:
+    """16 groups x 4 forks; each group shares one physical 120k-token prefix.
+
+    ``extra`` records the grouping: requests [g*forks, (g+1)*forks) share the
+    ``prefix_pages`` first pages.
+    """
     if prefix % PAGE_SIZE:
         raise ValueError("shared prefix must fill whole pages")
     rng = np.random.default_rng(seed)
     suffix = rng.lognormal(math.log(suffix_median), suffix_sigma, size=groups * forks)
-    suffix = np.clip(np.rint(suffix), 1, suffix_max).astype(np.int64)
+    suffix = np.clip(np.rint(suffix), num_queries, suffix_max).astype(np.int64)
     parts = []
     for g in range(groups):
         for f in range(forks):
             b = g * forks + f
             parts.append([(("prefix", g), prefix), (("suffix", b), int(suffix[b]))])
-    return _assemble("prefix_shared", seed, rng, 1, 64, parts,
-                     f"B={groups * forks} ({groups}x{forks} forks) H=64 Q=1 "
-                     f"prefix={prefix} suffix~logN(median {suffix_median:g}, sigma {suffix_sigma})")
+    w = _assemble("prefix_shared", seed, rng, num_queries, num_heads, parts,
+                  f"B={groups * forks} ({groups}x{forks} forks) H={num_heads} Q={num_queries} "
+                  f"prefix={prefix} suffix~logN(median {suffix_median:g}, sigma {suffix_sigma})")
+    w.extra = {"forks": forks, "prefix_pages": np.full(groups, prefix // PAGE_SIZE, np.int32)}
+    return w
 
 
 def speculative(seed: int = 4, batch: int = 32, num_queries: int = 4,

@@ -82,3 +82,16 @@ def test_workspace_size_grows_with_ctas(lib):
     # per piece: 64 heads x (512 + 1) floats
     assert b - a >= 100 * 64 * 513 * 4
     assert lib.mla_decode_workspace_size(1, 9, 64, 100) == 0
+
+
+def test_grouped_decode_checks_group_shape(lib):
+    """Group shapes the grouped decode cannot cut are refused before any launch."""
+    fake = ctypes.c_void_p(1 << 20)        # never dereferenced: the checks fail first
+    args = lambda batch, forks, ctas: (fake, fake, 100, 64, 0, fake, 4, fake, batch, 1, 64,
+                                       forks, fake, 0.1, 1.0, ctas, fake, 1 << 30, fake, fake,
+                                       None)
+    assert lib.mla_decode_grouped(*args(8, 3, 16)) == 1      # batch not a multiple of forks
+    assert lib.mla_decode_grouped(*args(8, 8, 4)) == 1       # more forks than CTAs
+    assert lib.mla_decode_grouped(*args(8, 0, 16)) == 1      # no forks
+    assert lib.mla_decode_grouped_workspace_size(8, 1, 64, 16) > \
+        lib.mla_decode_workspace_size(8, 1, 64, 16)
