@@ -53,7 +53,8 @@ cudaError_t launch_decode_tensor_core(const DecodeLaunch& d, cudaStream_t stream
 // decode kernel, which reads it.
 cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream);
 
-// Merge the pieces written by a decode kernel into out (bf16) and lse (fp32).
+// Merge the pieces written by a decode kernel into out (bf16) and lse (fp32);
+// max_pieces_per_row is the number of decode CTAs (it sizes the staging).
 cudaError_t launch_combine_pieces(const DecodeWorkspace& ws, int rows, int heads,
                                   int max_pieces_per_row, __nv_bfloat16* out, float* lse,
                                   cudaStream_t stream);

@@ -97,6 +97,16 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// Contiguous bulk copy global -> shared (both 16-byte aligned, bytes a multiple
+// of 16); completion is signalled on `mbar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+
 // Asks the memory system to bring [p, p + bytes) into L2 (no completion signal).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
