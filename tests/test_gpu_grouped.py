@@ -41,7 +41,7 @@ def _grouped(w, pages, dev, prefix_pages, forks, num_ctas=0, seq_lens=None, bloc
 
 @pytest.mark.parametrize("groups,forks,prefix,num_ctas", [
     (3, 4, 640, 0), (3, 4, 640, 12), (3, 4, 640, 13), (2, 3, 1280, 7), (4, 2, 64, 0),
-    (1, 8, 2048, 0), (2, 4, 640, 4), (5, 1, 320, 0)])
+    (1, 8, 2048, 0), (2, 4, 640, 4), (5, 1, 320, 0), (3, 4, 1280, 400)])
 def test_groups_match_oracle(cuda_device, groups, forks, prefix, num_ctas):
     w = wl.prefix_shared(seed=50 + groups + forks, groups=groups, forks=forks, prefix=prefix,
                          suffix_median=150.0, suffix_max=700)
@@ -54,9 +54,11 @@ def test_groups_match_oracle(cuda_device, groups, forks, prefix, num_ctas):
     assert_close(out, lse, ref_out, ref_lse, what=f"{groups}x{forks} prefix {prefix} G={num_ctas}")
 
 
-@pytest.mark.parametrize("nq", [2, 4])
-def test_groups_with_drafts(cuda_device, nq):
-    w = wl.prefix_shared(seed=60 + nq, groups=2, forks=4, prefix=1024, suffix_median=90.0,
+@pytest.mark.parametrize("nq,prefix,suffix", [(2, 1024, 90.0), (4, 1024, 90.0), (4, 16384, 8.0)])
+def test_groups_with_drafts(cuda_device, nq, prefix, suffix):
+    """Drafts see the shared prefix and their own causal suffix; the last case has
+    suffixes of a few tokens, so the four drafts' rows differ only in the last page."""
+    w = wl.prefix_shared(seed=60 + nq, groups=2, forks=4, prefix=prefix, suffix_median=suffix,
                          suffix_max=400, num_queries=nq)
     pages = gpu_fill_cache(w, cuda_device)
     ref_pages = oracle_fill_cache(w)
