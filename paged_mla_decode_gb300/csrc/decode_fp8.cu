@@ -17,24 +17,28 @@
 // small kernel launched before the decode kernel (q_split_kernel), which writes
 // the A operand in the order the decode kernel's threads load it. P = 2^(s - m + 6) is split into
 // an e4m3 term and an e5m2 remainder (7 significant bits; the e5m2 range keeps
-// tokens down to 2^-24 of the running maximum). All heads attend over the one latent
+// tokens down to about 2^-17 of the page's largest weight). All heads attend over the one latent
 // head ("vLLM x AgentX", section "Kimi K3"), so one page serves 64 heads, and V
 // is read in place through an MN-major descriptor (no distinct values: "How to
 // serve trillions of tokens ...", section "First, understand the workload").
 //
-// Warp roles (224 threads):
-//   warps 0-3  q loading, softmax and epilogue. Row t of A and S is (head
-//              16*(t/32) + t%16, part (t/16)%2), part 0 = hi, 1 = lo. Thread t
-//              handles head 16*(t/32) + t%16 and tokens 32*((t/16)%2) .. +31 of a
-//              page: it reads both terms' rows of its half-page (a half-split
-//              TMEM load), so no exchange between threads is needed; for O^T
-//              lane t is dim t of each 128-dim block.
-//   warp 4     TMA producer (lane 0): page ids from the block table a window of
+// Warp roles (416 threads):
+//   warps 0-7  q loading, softmax and epilogue. Row t of A and S is (head
+//              16*(t/32) + t%16, part (t/16)%2), part 0 = hi, 1 = lo. Warp w reads
+//              TMEM lanes 32*(w%4) .. +31; thread (w, lane) handles head
+//              16*(w%4) + lane%16 and the 16 tokens 32*(w/4) + 16*(lane/16) .. +15
+//              of a page, both terms (half-split TMEM loads of the hi and lo rows).
+//              A head's four threads agree on its page maximum through shared
+//              memory at the page's one block barrier. For O^T, lane t is dim t of
+//              each 128-dim block and warp w writes heads 32*(w/4) .. +31.
+//   warp 8     TMA producer (lane 0): page ids from the block table a window of
 //              pages ahead, pages into a ring of kRing shared-memory slots
 //              (128-byte swizzled latent blocks, 64-byte swizzled rope block).
-//   warp 5     TMEM allocation; issues QK (lane 0) after zeroing the rows of a
-//              partial page past its last token.
-//   warp 6     issues PV (lane 0).
+//   warps 9-10 issue QK of even / odd pages (lane 0); warp 9 allocates TMEM.
+//   warps 11-12 issue PV of even / odd pages (lane 0).
+// A thread that issues MMAs stalls for a while after each batch (until the
+// tensor pipe's queue has room), so two issuers per contraction keep the pipe
+// fed: one issues while the other waits.
 // TMEM (512 columns): A latent part [0,128), S buffers [128,192) [192,256),
 // O^T [256,512). The rope part of A is in shared memory.
 //
@@ -50,13 +54,29 @@
 #include "mla_internal.h"
 #include "tc_ptx.cuh"
 
+// Clock-stamp points of the pipeline: nothing unless a tracing build defines
+// MLA_STAMP(point, page) to record the SM clock there.
+#ifndef MLA_STAMP
+#define MLA_STAMP(point, page) ((void)0)
+#endif
+
 namespace mla {
 namespace {
 
-constexpr int kThreads = 224;
-constexpr int kTmaWarp = 4;
-constexpr int kQkWarp = 5;   // allocates TMEM, issues QK
-constexpr int kPvWarp = 6;   // issues PV
+enum StampPoint {
+  kStEntry, kStPrologue, kStTmaIssue, kStQkPage, kStQkIssued, kStSmS, kStSmBar, kStSmP,
+  kStPvP, kStPvIssued, kStEpiStart, kStEpiEnd, kStExit, kStQkGo, kStQkMma, kStQkTop
+};
+
+constexpr int kSmWarps = 8;                          // softmax / epilogue warps
+constexpr int kSmThreads = 32 * kSmWarps;            // 256
+constexpr int kTmaWarp = kSmWarps;                   // 8
+// MMA issuers: two QK warps and two PV warps, each issuing every other page
+// (page k goes to warp k % 2 of its kind), so that one warp's stall after a batch
+// of MMAs (an issuing thread waits on its MMA queue) overlaps the other's issue.
+constexpr int kQkWarp0 = kSmWarps + 1;               // 9: also allocates TMEM
+constexpr int kPvWarp0 = kSmWarps + 3;               // 11
+constexpr int kThreads = 32 * (kSmWarps + 5);        // 416
 constexpr int kRing = 5;                             // pages in flight
 constexpr int kPageBytes = kPageSize * kDEntry;      // 36864
 constexpr int kLatBlock = kPageSize * 128;           // 8192: 64 rows x 128 dims
@@ -91,41 +111,54 @@ constexpr int kOffPages = 0;
 constexpr int kOffQRope = kOffPages + kRing * kPageBytes;   // 128 rows x 64 B, 64B swizzle
 constexpr int kPBufs = 3;                                   // P^T buffers (QK runs 2 pages ahead)
 constexpr int kOffP = kOffQRope + 128 * 64;                 // [kPBufs] P^T buffers
-constexpr int kOffAlpha = kOffP + kPBufs * kPBytes;         // float [2][64]
-constexpr int kOffLinv = kOffAlpha + 512;                   // float [64]
-constexpr int kOffFlags = kOffLinv + 256;                   // int [4]
+constexpr int kOffAlpha = kOffP + kPBufs * kPBytes;         // float [64]
+constexpr int kOffLinv = kOffAlpha + 256;                   // float [64]
+constexpr int kOffPmax = kOffLinv + 256;                    // float [2 pages][2 halves][64]
+constexpr int kOffLsum = kOffPmax + 1024;                   // float [2 halves][64]
+constexpr int kOffFlags = kOffLsum + 512;                   // int [4]
 constexpr int kOffPlan = kOffFlags + 16;                    // int64 [6]
 constexpr int kDescRing = 64;                               // page descriptors in flight
 constexpr int kTableAhead = 32;  // pages described (block-table read started) before issue
 constexpr int kOffDesc = kOffPlan + 48;                     // PageDesc [kDescRing]
 constexpr int kOffBar = kOffDesc + 16 * kDescRing;
-constexpr int BAR_PAGE_FULL = 0;              // [kRing] TMA bytes (or zero fill) landed
-constexpr int BAR_PAGE_EMPTY = kRing;         // [kRing] PV of the slot's page finished
-constexpr int BAR_S_FULL = 2 * kRing;         // [2] page j: buffer j % 2
-constexpr int BAR_S_EMPTY = 2 * kRing + 2;    // [2] (4 softmax warps)
-constexpr int BAR_P_FULL = 2 * kRing + 4;     // [kPBufs] page j: buffer j % 3 (4 softmax warps)
-constexpr int BAR_PV_DONE = 2 * kRing + 7;    // [2] PV of page j commits barrier j % 2
-constexpr int BAR_O_FULL = 2 * kRing + 9;
-constexpr int BAR_O_EMPTY = 2 * kRing + 10;   // (4 softmax warps)
-constexpr int BAR_Q_READY = 2 * kRing + 11;   // (4 softmax warps)
-constexpr int BAR_Q_EMPTY = 2 * kRing + 12;
-constexpr int BAR_DRAIN = 2 * kRing + 13;      // [2] QK warp, PV warp
-constexpr int BAR_P_EMPTY = 2 * kRing + 15;    // [kPBufs] PV of page j read P buffer j % 3
+constexpr int BAR_PAGE_FULL = 0;                  // [kRing] TMA bytes (or zero fill) landed
+// PV(k) completes barrier BAR_PV_DONE + k % kRing (one commit per page): it frees
+// page slot k % kRing for the TMA warp, P buffer k % 3 for the softmax warps, and
+// marks O^T current for a rescale. Every wait on it names a page whose successor
+// on the same barrier (k + kRing) cannot have completed yet, so parities are exact.
+constexpr int BAR_PV_DONE = kRing;                // [kRing]
+constexpr int BAR_S_FULL = 2 * kRing;             // [2] page j: buffer j % 2
+constexpr int BAR_S_EMPTY = BAR_S_FULL + 2;       // [2] (softmax warps)
+constexpr int BAR_P_FULL = BAR_S_EMPTY + 2;       // [kPBufs] page j: buffer j % 3 (softmax warps)
+constexpr int BAR_O_FULL = BAR_P_FULL + kPBufs;
+constexpr int BAR_O_EMPTY = BAR_O_FULL + 1;       // (softmax warps)
+constexpr int BAR_Q_READY = BAR_O_EMPTY + 1;      // (softmax warps)
+constexpr int BAR_Q_EMPTY = BAR_Q_READY + 1;
+constexpr int BAR_DRAIN = BAR_Q_EMPTY + 1;       // [4] one per issuer warp
 #ifdef MLA_TEST_STALL_QK
-// Test build only: a barrier that nothing ever completes. The QK issuer waits on
-// it before its third page, so the wait runs out and the CTA takes the timeout
-// path (stop every role, drain the copies and MMAs in flight, free TMEM).
-constexpr int BAR_TEST_STALL = 2 * kRing + 15 + kPBufs;
+// Test build only: a barrier that nothing ever completes. The MMA issuer waits on
+// it before the QK of its third page, so the wait runs out and the CTA takes the
+// timeout path (stop every role, drain the copies and MMAs in flight, free TMEM).
+constexpr int BAR_TEST_STALL = BAR_DRAIN + 4;
 constexpr int kNumBars = BAR_TEST_STALL + 1;
 #else
-constexpr int kNumBars = 2 * kRing + 15 + kPBufs;
+constexpr int kNumBars = BAR_DRAIN + 4;
 #endif
+// arrivals that complete a phase of barrier i
+__device__ __forceinline__ uint32_t bar_count(int i) {
+  if ((i >= BAR_S_EMPTY && i < BAR_S_EMPTY + 2) || (i >= BAR_P_FULL && i < BAR_P_FULL + kPBufs) ||
+      i == BAR_O_EMPTY || i == BAR_Q_READY)
+    return kSmWarps;
+  if (i == BAR_Q_EMPTY || i == BAR_O_FULL) return 2;  // both issuer warps of the kind commit
+  return 1;
+}
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024 alignment
 // grouped decode: the two segments' plans (int64 [32]) after the common map
 constexpr int kOffPlanX = (kSmemUsed + 15) & ~15;
 constexpr int kSmemBytesGrouped = kOffPlanX + 256 + 1024;
+static_assert(kSmemBytesGrouped <= 227 * 1024, "shared memory map exceeds 227 KB");
 
 enum Flag { F_ABORT = 0, F_PIECE_BAD = 1 };
 
@@ -243,15 +276,15 @@ struct SegWalker : PageWalker<GroupPlan> {
 };
 
 __device__ __forceinline__ void named_bar_softmax() {
-  asm volatile("bar.sync 1, 128;\n" ::: "memory");
+  asm volatile("bar.sync 1, %0;\n" ::"n"(kSmThreads) : "memory");
 }
 __device__ __forceinline__ bool named_bar_softmax_or(bool pred) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 128, p;\n"
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
       " selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)pred)
+      : "r"((uint32_t)pred), "n"(kSmThreads)
       : "memory");
   return r != 0;
 }
@@ -285,22 +318,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (sbase - raw_a);
   float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
   float* linv_s = reinterpret_cast<float*>(smem + kOffLinv);
+  float* pmax_s = reinterpret_cast<float*>(smem + kOffPmax);
+  float* lsum_s = reinterpret_cast<float*>(smem + kOffLsum);
   volatile int* flags = reinterpret_cast<volatile int*>(smem + kOffFlags);
   int64_t* s_plan = reinterpret_cast<int64_t*>(smem + kOffPlan);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   auto bar = [&](int i) -> uint32_t { return sbase + kOffBar + 8u * (uint32_t)i; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) MLA_STAMP(kStEntry, 0);
 
   // ---- planning (shared by all roles) ----
   // This kernel starts once the query split kernel before it has passed its own
   // wait for all earlier work in the stream (see launch_decode_fp8), so the
   // lengths, block table and pages may be read at once; only the split query
   // itself needs the split kernel to have completed (griddep_wait before q_op).
-  if (warp == kTmaWarp && lane == 0) {
-    tc::prefetch_tensormap(&lat_map);
-    tc::prefetch_tensormap(&rope_map);
-  }
   Plan plan{p.seq_lens, p.batch, p.nq, p.max_pages, kPageSize, p.G, 0};
   const int c = blockIdx.x;
   int64_t* s_plan_x = reinterpret_cast<int64_t*>(smem + kOffPlanX);  // kGrouped only
@@ -342,18 +374,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  if (warp == kPvWarp && lane == 0) {
-    for (int i = 0; i < kNumBars; ++i) {
-      const bool by_warps = (i >= BAR_S_EMPTY && i < BAR_S_EMPTY + 2) ||
-                            (i >= BAR_P_FULL && i < BAR_P_FULL + kPBufs) || i == BAR_O_EMPTY ||
-                            i == BAR_Q_READY;
-      tc::mbar_init(bar(i), by_warps ? 4 : 1);
-    }
+  if (warp == kTmaWarp && lane == 0) {
+    tc::prefetch_tensormap(&lat_map);
+    tc::prefetch_tensormap(&rope_map);
+    for (int i = 0; i < kNumBars; ++i) tc::mbar_init(bar(i), bar_count(i));
     tc::fence_mbar_init();
     flags[F_ABORT] = 0;
     flags[F_PIECE_BAD] = 0;
   }
-  if (warp == kQkWarp) {
+  if (warp == kQkWarp0) {
     tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tc::tmem_relinquish();
   }
@@ -361,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   griddep_launch_dependents();  // the combine kernel may be scheduled (it waits for this grid)
+  if (tid == 0) MLA_STAMP(kStPrologue, 0);
   int64_t x_begin = 0, x_end = 0;
   if constexpr (kGrouped) {
     x_end = s_plan[0];
@@ -381,6 +411,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int64_t npages = x_end - x_begin;
   const PageDesc* desc = reinterpret_cast<const PageDesc*>(smem + kOffDesc);
+  // This CTA's walk over its pages (the TMA lane describes each page from it; the
+  // MMA issuers follow their own copy for the piece boundaries, in registers).
+  using Walker = std::conditional_t<kGrouped, SegWalker, PageWalker<Plan>>;
+  auto start_walker = [&](Walker& pw) {
+    if constexpr (kGrouped) {
+      GroupPlan A = group_plan(p, 1), B = group_plan(p, 2);
+      A.set_total(s_plan_x[0]);
+      B.set_total(s_plan_x[1]);
+      const RowCursor ca{(int)s_plan_x[8], s_plan_x[9], (int)s_plan_x[10], (int)s_plan_x[11],
+                         (int)s_plan_x[12]};
+      const RowCursor cb{(int)s_plan_x[13], s_plan_x[14], (int)s_plan_x[15], (int)s_plan_x[16],
+                         (int)s_plan_x[17]};
+      pw.start(A, ca, s_plan_x[2], s_plan_x[3], (int)s_plan_x[6], (int)s_plan_x[7], B, cb,
+               s_plan_x[4], s_plan_x[5], c, p.ws.row_base, p.ws.row_np1);
+    } else {
+      pw.init(plan, cur0, c, x_begin, x_end);
+    }
+  };
   if (x_begin < x_end) {
     if (warp == kTmaWarp) {
       // =================== TMA producer (lane 0) ===================
@@ -392,20 +440,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const uint64_t pol = l2_evict_first_policy();
         PageDesc* ring = reinterpret_cast<PageDesc*>(smem + kOffDesc);
-        std::conditional_t<kGrouped, SegWalker, PageWalker<Plan>> pw;
-        if constexpr (kGrouped) {
-          GroupPlan A = group_plan(p, 1), B = group_plan(p, 2);
-          A.set_total(s_plan_x[0]);
-          B.set_total(s_plan_x[1]);
-          const RowCursor ca{(int)s_plan_x[8], s_plan_x[9], (int)s_plan_x[10],
-                             (int)s_plan_x[11], (int)s_plan_x[12]};
-          const RowCursor cb{(int)s_plan_x[13], s_plan_x[14], (int)s_plan_x[15],
-                             (int)s_plan_x[16], (int)s_plan_x[17]};
-          pw.start(A, ca, s_plan_x[2], s_plan_x[3], (int)s_plan_x[6], (int)s_plan_x[7], B, cb,
-                   s_plan_x[4], s_plan_x[5], c, p.ws.row_base, p.ws.row_np1);
-        } else {
-          pw.init(plan, cur0, c, x_begin, x_end);
-        }
+        Walker pw;
+        start_walker(pw);
         int64_t jn = 0;  // next page to describe
         auto describe_next = [&]() {
           PageDesc& d = ring[jn % kDescRing];
@@ -439,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t round = (uint32_t)(j / kRing);
           const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
           if (j >= kRing &&
-              (!tc::mbar_wait(bar(BAR_PAGE_EMPTY + slot), (round - 1) & 1, kWaitNs) ||
+              (!tc::mbar_wait(bar(BAR_PV_DONE + slot), (round - 1) & 1, kWaitNs) ||
                flags[F_ABORT])) {
             ok = false;
             break;
@@ -455,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    bar(BAR_PAGE_FULL + slot), pol);
             tc::tma_load_2d_hint(page_base + kRopeOff, &rope_map, kDLatent, y,
                                  bar(BAR_PAGE_FULL + slot), pol);
+            MLA_STAMP(kStTmaIssue, j);
           } else {
             tc::mbar_arrive(bar(BAR_PAGE_FULL + slot));  // bad id: the MMA warp zero-fills
           }
@@ -468,154 +505,155 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kDrainWaitNs);
       }
       __syncwarp();
-    } else if (warp == kQkWarp || warp == kPvWarp) {
-      // ============ MMA issuers: QK warp and PV warp, lane 0 issues ============
-      // The two streams are issued by different threads, so neither's completion
-      // implies the other's: P buffer reuse and the O^T rescale wait on the PV
-      // warp's own commits (P_EMPTY, PV_DONE).
+    } else if (warp >= kQkWarp0) {
+      // ============ MMA issuers: two QK warps, two PV warps; lane 0 issues ============
+      // Page k's QK is issued by QK warp k % 2 (into S buffer k % 2, which is that
+      // warp's own) and its PV by PV warp k % 2. MMAs of different threads complete
+      // in no particular order relative to each other, so every wait names the page
+      // it needs (PV_DONE per page) and the once-per-piece barriers count both warps
+      // of a kind: each passes every piece start (QK: the piece's q is loaded; PV:
+      // O^T is zero) and commits at every piece end (Q_EMPTY, O_FULL), whether or not
+      // it issued a page of that piece. PV always accumulates: the softmax warps zero
+      // O^T before a piece starts. A PV issues its e4m3 (hi) MMAs before its e5m2
+      // (lo) ones: MMAs that alternate B formats run at half rate.
       constexpr uint32_t id_qk = tc::idesc_f8(128, 64, tc::kFmtE4M3, tc::kFmtE4M3, false, false);
       // PV: A = V^T (e4m3, MN-major); B = P^T hi (e4m3) or lo (e5m2), K-major
       constexpr uint32_t id_pv_hi = tc::idesc_f8(128, 64, tc::kFmtE4M3, tc::kFmtE4M3, true, false);
       constexpr uint32_t id_pv_lo = tc::idesc_f8(128, 64, tc::kFmtE4M3, tc::kFmtE5M2, true, false);
-      const bool leader = lane == 0;
-      // bounded wait by lane 0, result shared with the warp
-      auto wait0 = [&](int b, uint32_t parity) -> bool {
-        bool got = true;
-        if (leader) got = tc::mbar_wait(bar(b), parity, kWaitNs);
-        return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-      };
-      bool ok = true;
-      if (warp == kQkWarp) {
+      const bool is_qk = warp < kPvWarp0;
+      const int mine = warp - (is_qk ? kQkWarp0 : kPvWarp0);  // pages k with k % 2 == mine
+      // Only lane 0 runs the issue loop: MMA issue stalls while the tensor pipe's
+      // queue is full, so any other work between batches (warp votes, shuffles,
+      // warp barriers) leaves the pipe idle.
+      if (lane == 0) {
+        auto wait = [&](int b, uint32_t parity) -> bool {
+          return tc::mbar_wait(bar(b), parity, kWaitNs);
+        };
         const uint64_t qrope_desc = tc::smem_desc(sbase + kOffQRope, 16, 512, tc::kSwizzle64);
-        int q_piece = 0;
-        for (int64_t k = 0; k < npages && ok; ++k) {
-          if (flags[F_ABORT]) {
+        int piece_n = 0;
+        bool ok = true;
+        Walker pw;  // piece boundaries without reading the shared descriptors
+        start_walker(pw);
+        for (int64_t k = 0; k < npages && ok; ++k, pw.next()) {
+          // (another role's stop is seen here every 8 pages, or as a wait that runs out)
+          if ((k & 7) == 0 && flags[F_ABORT]) {
             ok = false;
             break;
           }
-#ifdef MLA_TEST_STALL_QK
-          if (k == 2) {
-            ok = wait0(BAR_TEST_STALL, 0);
-            if (!ok) break;
-          }
-#endif
-          const int slot = (int)(k % kRing);
-          const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
-          ok = wait0(BAR_PAGE_FULL + slot, (uint32_t)(k / kRing) & 1);
-          if (!ok) break;
-          const PageDesc d = desc[k % kDescRing];
-          if (d.flags & kDescPieceStart) {
-            ok = wait0(BAR_Q_READY, (uint32_t)q_piece & 1);
-            ++q_piece;
-          }
-          if (ok && k >= 2) ok = wait0(BAR_S_EMPTY + (int)(k & 1), (uint32_t)((k >> 1) - 1) & 1);
-          if (!ok) break;
-          // rows past the page's last token (all rows of a bad page id) become zeros,
-          // so that masked tokens contribute 0 * finite to PV
-          const int zero_from = (d.flags & kDescPageOk) ? d.valid : 0;
-          if (zero_from < kPageSize) {
-            for (int i = lane; i < (kPageSize - zero_from) * 36; i += 32) {
-              const int row = zero_from + i / 36, u = i % 36;
-              const uint32_t a = u < 32 ? page_base + (u >> 3) * kLatBlock + row * 128 + (u & 7) * 16
-                                        : page_base + kRopeOff + row * 64 + (u - 32) * 16;
-              asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(a), "r"(0u));
-            }
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-          }
-          if (leader) {
-            // ---- S = A . page^T: latent part of A from TMEM, rope from shared memory ----
-            tc::fence_after_sync();
-            const uint64_t kb = tc::smem_desc(page_base, 16, 1024, tc::kSwizzle128);
-            const uint64_t rb = tc::smem_desc(page_base + kRopeOff, 16, 512, tc::kSwizzle64);
-            const uint32_t d_s = tmem + s_col((int)(k & 1));
-#pragma unroll
-            for (int s = 0; s < 16; ++s)
-              tc::mma_f8_ts(d_s, tmem + kQCol + 8 * s,
-                            kb + (uint64_t)(((s >> 2) * kLatBlock + (s & 3) * 32) >> 4), id_qk,
-                            s > 0);
-#pragma unroll
-            for (int s = 0; s < 2; ++s)
-              tc::mma_f8_ss(d_s, qrope_desc + (uint64_t)((32 * s) >> 4),
-                            rb + (uint64_t)((32 * s) >> 4), id_qk, 1);
-            tc::mma_commit(bar(BAR_S_FULL + (int)(k & 1)));
-            if (d.flags & kDescPieceEnd) tc::mma_commit(bar(BAR_Q_EMPTY));
-          }
-          __syncwarp();
-        }
-      } else {
-        int o_piece = 0;
-        for (int64_t k = 0; k < npages && ok; ++k) {
-          if (flags[F_ABORT]) {
-            ok = false;
-            break;
-          }
-          const int pb_i = (int)(k % kPBufs);
-          ok = wait0(BAR_P_FULL + pb_i, (uint32_t)(k / kPBufs) & 1);
-          if (!ok) break;
-          const PageDesc d = desc[k % kDescRing];
-          const bool ps = d.flags & kDescPieceStart, pe = d.flags & kDescPieceEnd;
+          const bool ps = pw.piece_start(), pe = pw.piece_end();
           if (ps) {
-            if (o_piece > 0) ok = wait0(BAR_O_EMPTY, (uint32_t)(o_piece - 1) & 1);
-            ++o_piece;
+            ok = wait(is_qk ? BAR_Q_READY : BAR_O_EMPTY, (uint32_t)piece_n & 1);
+            ++piece_n;
             if (!ok) break;
           }
-          if (leader) {
-            // ---- O^T += V^T P^T ----
-            tc::fence_after_sync();
+          if ((int)(k & 1) == mine) {
             const int slot = (int)(k % kRing);
             const uint32_t page_base = sbase + kOffPages + slot * kPageBytes;
-            const uint64_t va = tc::smem_desc(page_base, kLatBlock, 1024, tc::kSwizzle128);
-            const uint64_t pb =
-                tc::smem_desc(sbase + kOffP + pb_i * kPBytes, 16, 1024, tc::kSwizzle128);
+            if (is_qk) {
+              // ---- S(k) = A . page(k)^T: latent part of A from TMEM, rope from shared memory ----
+#ifdef MLA_TEST_STALL_QK
+              if (k == 2 && !wait(BAR_TEST_STALL, 0)) {
+                ok = false;
+                break;
+              }
+#endif
+              MLA_STAMP(kStQkTop, k);
+              ok = wait(BAR_PAGE_FULL + slot, (uint32_t)(k / kRing) & 1);
+              MLA_STAMP(kStQkPage, k);
+              // S buffer k % 2 last held S(k - 2), issued by this warp
+              if (ok && k >= 2) ok = wait(BAR_S_EMPTY + (int)(k & 1), (uint32_t)((k >> 1) - 1) & 1);
+              if (!ok) break;
+              MLA_STAMP(kStQkGo, k);
+              tc::fence_after_sync();
+              const uint64_t kb = tc::smem_desc(page_base, 16, 1024, tc::kSwizzle128);
+              const uint64_t rb = tc::smem_desc(page_base + kRopeOff, 16, 512, tc::kSwizzle64);
+              const uint32_t d_s = tmem + s_col((int)(k & 1));
 #pragma unroll
-            for (int blk = 0; blk < 4; ++blk)
+              for (int s = 0; s < 16; ++s)
+                tc::mma_f8_ts(d_s, tmem + kQCol + 8 * s,
+                              kb + (uint64_t)(((s >> 2) * kLatBlock + (s & 3) * 32) >> 4), id_qk,
+                              s > 0);
 #pragma unroll
               for (int s = 0; s < 2; ++s)
+                tc::mma_f8_ss(d_s, qrope_desc + (uint64_t)((32 * s) >> 4),
+                              rb + (uint64_t)((32 * s) >> 4), id_qk, 1);
+              MLA_STAMP(kStQkMma, k);
+              tc::mma_commit(bar(BAR_S_FULL + (int)(k & 1)));
+              MLA_STAMP(kStQkIssued, k);
+            } else {
+              // ---- O^T += V^T P^T (V read in place through an MN-major descriptor) ----
+              const int pb_i = (int)(k % kPBufs);
+              ok = wait(BAR_P_FULL + pb_i, (uint32_t)(k / kPBufs) & 1);
+              if (!ok) break;
+              MLA_STAMP(kStPvP, k);
+              tc::fence_after_sync();
+              const uint64_t va = tc::smem_desc(page_base, kLatBlock, 1024, tc::kSwizzle128);
+              const uint64_t pb =
+                  tc::smem_desc(sbase + kOffP + pb_i * kPBytes, 16, 1024, tc::kSwizzle128);
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
-                  tc::mma_f8_ss(tmem + kOCol + 64 * blk,
-                                va + (uint64_t)((blk * kLatBlock + s * 4096) >> 4),
-                                pb + (uint64_t)((64 * part + 32 * s) >> 4),
-                                part ? id_pv_lo : id_pv_hi, !(ps && s == 0 && part == 0));
-            tc::mma_commit(bar(BAR_PAGE_EMPTY + slot));
-            tc::mma_commit(bar(BAR_P_EMPTY + pb_i));
-            tc::mma_commit(bar(BAR_PV_DONE + (int)(k & 1)));
-            if (pe) tc::mma_commit(bar(BAR_O_FULL));
+              for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int blk = 0; blk < 4; ++blk)
+#pragma unroll
+                  for (int s = 0; s < 2; ++s)
+                    tc::mma_f8_ss(tmem + kOCol + 64 * blk,
+                                  va + (uint64_t)((blk * kLatBlock + s * 4096) >> 4),
+                                  pb + (uint64_t)((64 * part + 32 * s) >> 4),
+                                  part ? id_pv_lo : id_pv_hi, 1);
+              tc::mma_commit(bar(BAR_PV_DONE + slot));
+              MLA_STAMP(kStPvIssued, k);
+            }
           }
-          __syncwarp();
+          if (pe) tc::mma_commit(bar(is_qk ? BAR_Q_EMPTY : BAR_O_FULL));
         }
-      }
-      if (leader) {
         if (!ok) abort_cta();
         // drain: every MMA this thread issued has finished before TMEM is freed
-        const int db = BAR_DRAIN + (warp == kPvWarp ? 1 : 0);
+        const int db = BAR_DRAIN + (warp - kQkWarp0);
         tc::mma_commit(bar(db));
-        if (!tc::mbar_wait(bar(db), 0, kDrainWaitNs))
-          atomicOr(p.ws.status, MLA_DEVICE_ERR_TIMEOUT);
+        if (!tc::mbar_wait(bar(db), 0, kDrainWaitNs)) atomicOr(p.ws.status, MLA_DEVICE_ERR_TIMEOUT);
       }
       __syncwarp();
     } else {
-      // =================== softmax + epilogue (warps 0-3) ===================
+      // =================== softmax + epilogue (warps 0-7) ===================
+      // Warp w reads TMEM lanes 32*(w%4) .. +31 (rows of A and S; dims of O^T) and
+      // handles half g = w/4 of each page: thread (w, lane) owns head
+      // h = 16*(w%4) + lane%16 and the 16 tokens 32*g + 16*(lane/16) .. +15, both
+      // q terms of each (a half-split TMEM load of the hi rows and of the lo rows).
+      // A head's four threads agree on its running maximum through shared memory
+      // at the one block barrier of each page; each keeps its own part of the sum.
       const int t = tid;
-      const int h = 16 * warp + (lane & 15);   // head of this thread's row
-      const int part = (lane >> 4) & 1;        // 0: q_hi / tokens 0-31, 1: q_lo / tokens 32-63
-      const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-      float m = -INFINITY, l = 0.f, qmul = 0.f;
+      const int q4 = warp & 3, g = warp >> 2;
+      const int h = 16 * q4 + (lane & 15);
+      const int c16 = 2 * g + (lane >> 4);      // this thread's 16-token chunk of a page
+      const uint32_t lane_hi = (uint32_t)(32 * q4) << 16;
+      const uint32_t lane_lo = (uint32_t)(32 * q4 + 16) << 16;
+      float m = -INFINITY, lpart = 0.f, qmul = 0.f;
       int piece = 0;
       bool ok = true;
+      {
+        // O^T starts at zero (PV always accumulates); this warp's lanes, heads 32g ..
+        uint32_t zz[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) zz[i] = 0u;
+#pragma unroll
+        for (int blk = 0; blk < 4; ++blk) tc::tmem_st32(tmem + lane_hi + kOCol + 64 * blk + 32 * g, zz);
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bar(BAR_O_EMPTY));
+      }
       for (int64_t j = 0; j < npages; ++j) {
         // Page 0 opens the first piece, whose row the plan gives: its q is staged at
         // once. Later pages' descriptors are read once the page has landed.
         int row = cur0.r;
         bool ps = j == 0;
+        // (a failed wait is acted on at this page's block barrier below; every
+        // thread reads the same descriptor word, so the piece-start decision, and
+        // with it the barriers of the q staging, is uniform either way)
+        if (!tc::mbar_wait(bar(BAR_PAGE_FULL + (int)(j % kRing)), (uint32_t)(j / kRing) & 1,
+                           kWaitNs))
+          flags[F_ABORT] = 1;
         if (j > 0) {
-          // (a failed wait is acted on at this page's group barrier below; every
-          // thread reads the same descriptor word, so the piece-start decision, and
-          // with it the barriers of the q staging, is uniform either way)
-          if (!tc::mbar_wait(bar(BAR_PAGE_FULL + (int)(j % kRing)), (uint32_t)(j / kRing) & 1,
-                             kWaitNs))
-            flags[F_ABORT] = 1;
           const PageDesc d0 = desc[j % kDescRing];
           row = min(max(d0.row, 0), p.rows - 1);  // in range even if a stopped producer never wrote it
           ps = d0.flags & kDescPieceStart;
@@ -630,34 +668,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // The query split kernel wrote this row's operand as [36 chunks][128 lanes]
-          // [16 codes]: this thread loads the 36 chunks of its own lane (coalesced
-          // across the warp), stores the 32 latent chunks into its TMEM lane and the
-          // 4 rope chunks into its shared-memory row (64-byte swizzle).
+          // [16 codes]: TMEM lane r = 32*(w%4) + lane gets its 32 latent chunks (half
+          // g loads chunks 16g .. 16g+15) and its shared-memory row the 4 rope chunks
+          // (half g: 32 + 2g, 33 + 2g), 64-byte swizzled.
           griddep_wait();  // the split kernel has completed and its writes are visible
           const bool live = h < H;
           qmul = live ? __ldcg(p.ws.q_mul + (int64_t)row * 64 + h) : 0.f;
+          const int r = 32 * q4 + lane;
           const uint4* src =
-              reinterpret_cast<const uint4*>(p.ws.q_op + (int64_t)row * kQOpRowBytes) + t;
-          uint4 qc[kQOpChunks];
+              reinterpret_cast<const uint4*>(p.ws.q_op + (int64_t)row * kQOpRowBytes) + r;
+          uint4 qc[18];
 #pragma unroll
-          for (int u = 0; u < kQOpChunks; ++u)
-            qc[u] = live ? __ldcg(src + 128 * u) : make_uint4(0, 0, 0, 0);
+          for (int u = 0; u < 16; ++u)
+            qc[u] = live ? __ldcg(src + 128 * (16 * g + u)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
+          for (int u = 0; u < 2; ++u)
+            qc[16 + u] = live ? __ldcg(src + 128 * (32 + 2 * g + u)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int gg = 0; gg < 2; ++gg) {
             uint32_t v[32];
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              v[4 * k] = qc[8 * g + k].x;
-              v[4 * k + 1] = qc[8 * g + k].y;
-              v[4 * k + 2] = qc[8 * g + k].z;
-              v[4 * k + 3] = qc[8 * g + k].w;
+              v[4 * k] = qc[8 * gg + k].x;
+              v[4 * k + 1] = qc[8 * gg + k].y;
+              v[4 * k + 2] = qc[8 * gg + k].z;
+              v[4 * k + 3] = qc[8 * gg + k].w;
             }
-            tc::tmem_st32(tmem + lane_base + kQCol + 32 * g, v);
+            tc::tmem_st32(tmem + lane_hi + kQCol + 64 * g + 32 * gg, v);
           }
 #pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4) {
-            const uint32_t a = sbase + kOffQRope + t * 64 + ((c4 ^ ((t >> 1) & 3)) << 4);
-            const uint4 v = qc[32 + c4];
+          for (int u = 0; u < 2; ++u) {
+            const int c4 = 2 * g + u;
+            const uint32_t a = sbase + kOffQRope + r * 64 + ((c4 ^ ((r >> 1) & 3)) << 4);
+            const uint4 v = qc[16 + u];
             asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(a), "r"(v.x), "r"(v.y),
                          "r"(v.z), "r"(v.w));
           }
@@ -669,9 +712,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- S of this page ----
         // (a failed wait, like a stop by another role, is acted on at this page's
-        // group barrier below: one barrier per page)
+        // block barrier below: one barrier per page)
         if (!tc::mbar_wait(bar(BAR_S_FULL + (int)(j & 1)), (uint32_t)(j >> 1) & 1, kWaitNs))
           flags[F_ABORT] = 1;
+        if (t == 0) MLA_STAMP(kStSmS, j);
         // page validity (tokens of a bad page id are masked and reported)
         const PageDesc d = desc[j % kDescRing];
         const bool pe = d.flags & kDescPieceEnd;
@@ -682,92 +726,102 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicOr(p.ws.status, MLA_DEVICE_ERR_BAD_PAGE);
         }
         tc::fence_after_sync();
-        // both terms of this thread's 32 tokens: rows 32w .. 32w+15 hold q_hi . k of
-        // heads 16w .. 16w+15, rows 32w+16 .. 32w+31 q_lo . k; a half-warp reads
-        // one half of the page's 64 columns
-        uint32_t shi[32], slo[32];
-        tc::tmem_ld16x2_32(tmem + ((uint32_t)(32 * warp) << 16) + s_col((int)(j & 1)), shi);
-        tc::tmem_ld16x2_32(tmem + ((uint32_t)(32 * warp + 16) << 16) + s_col((int)(j & 1)), slo);
+        uint32_t shi[16], slo[16];
+        const uint32_t scol = s_col((int)(j & 1)) + 32u * (uint32_t)g;
+        tc::tmem_ld16x2_16(tmem + lane_hi + scol, shi);
+        tc::tmem_ld16x2_16(tmem + lane_lo + scol, slo);
         tc::tmem_wait_ld();
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(bar(BAR_S_EMPTY + (int)(j & 1)));
-        float s[32];
-        float tmax = -INFINITY;
+        float s[16];
+        float tm = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const bool vis = 32 * part + i < nvis;
+        for (int i = 0; i < 16; ++i) {
+          const bool vis = 16 * c16 + i < nvis;
           s[i] = vis ? (__uint_as_float(shi[i]) + __uint_as_float(slo[i])) * qmul : -INFINITY;
-          tmax = fmaxf(tmax, s[i]);
+          tm = fmaxf(tm, s[i]);
         }
-        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
-        // lazy running max: O is rescaled only when a head's page max rises more than
-        // kRescaleThresh above it or falls more than kLowThresh below it
-        float alpha = 1.f;
-        bool grow = false;
-        if (ps) {
-          m = tmax;
-        } else if (tmax > m + kRescaleThresh) {
-          alpha = m == -INFINITY ? 0.f : fast_exp2(m - tmax);
-          m = tmax;
-          l *= alpha;
-          grow = true;
-        } else if (tmax < m - kLowThresh && l * fast_exp2(m - tmax) <= kMassCap) {
-          alpha = fast_exp2(m - tmax);  // > 1: the page is far below the running max
-          m = tmax;
-          l *= alpha;
-          grow = true;
-        }
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+        if (lane < 16) pmax_s[(int)(j & 1) * 128 + g * 64 + h] = tm;
         // P buffer j % 3 was read by PV(j - 3); waiting for it also makes the
-        // PV_DONE parity below unambiguous (PV(j - 3) is complete)
+        // PV_DONE parity of the rescale below unambiguous (PV(j - 3) is complete)
         if (j >= kPBufs && !flags[F_ABORT]) {
-          const bool got = tc::mbar_wait(bar(BAR_P_EMPTY + (int)(j % kPBufs)),
-                                         (uint32_t)(j / kPBufs - 1) & 1, kWaitNs);
+          const int64_t jp = j - kPBufs;  // the page whose PV read this P buffer
+          const bool got = tc::mbar_wait(bar(BAR_PV_DONE + (int)(jp % kRing)),
+                                         (uint32_t)(jp / kRing) & 1, kWaitNs);
           if (!got) {
             flags[F_ABORT] = 1;
             atomicOr(p.ws.status, MLA_DEVICE_ERR_TIMEOUT);
           }
         }
-        float* alpha_w = alpha_s + 64 * (int)(j & 1);
-        if (part == 0) alpha_w[h] = alpha;
-        if (named_bar_softmax_or(grow || flags[F_ABORT] != 0)) {
-          // rare: a stop, or a head's max grew
-          if (named_bar_softmax_or(flags[F_ABORT] != 0)) {
-            ok = false;
-            break;
+        // lazy running max: O is rescaled only when a head's page max rises more than
+        // kRescaleThresh above it or falls more than kLowThresh below it; a half
+        // page's max outside that band asks every thread to look closer
+        const bool trig = !ps && (tm > m + kRescaleThresh || tm < m - kLowThresh);
+        const bool any = named_bar_softmax_or(trig || flags[F_ABORT] != 0);
+        if (t == 0) MLA_STAMP(kStSmBar, j);
+        const float tmax = fmaxf(tm, pmax_s[(int)(j & 1) * 128 + (1 - g) * 64 + h]);
+        if (any && named_bar_softmax_or(flags[F_ABORT] != 0)) {
+          ok = false;
+          break;
+        }
+        if (ps) {
+          m = tmax;
+        } else if (any) {
+          // rare: the exact decision per head, with the head's whole sum
+          const float lh = lpart + __shfl_xor_sync(0xffffffffu, lpart, 16);
+          if (lane < 16) lsum_s[g * 64 + h] = lh;
+          named_bar_softmax();
+          const float lhead = lsum_s[h] + lsum_s[64 + h];
+          float alpha = 1.f;
+          bool grow = false;
+          if (tmax > m + kRescaleThresh) {
+            alpha = m == -INFINITY ? 0.f : fast_exp2(m - tmax);
+            grow = true;
+          } else if (tmax < m - kLowThresh && lhead * fast_exp2(m - tmax) <= kMassCap) {
+            alpha = fast_exp2(m - tmax);  // > 1: the page is far below the running max
+            grow = true;
           }
-          // bring O^T (PV of the previous page done) to the new maxima (up or down)
-          const bool got =
-              tc::mbar_wait(bar(BAR_PV_DONE + (int)((j - 1) & 1)), (uint32_t)((j - 1) >> 1) & 1,
-                            kWaitNs);
-          if (named_bar_softmax_or(!got)) {
-            ok = false;
-            break;
+          if (grow) {
+            m = tmax;
+            lpart *= alpha;
           }
-          tc::fence_after_sync();
+          if (g == 0 && lane < 16) alpha_s[h] = alpha;
+          if (named_bar_softmax_or(grow)) {
+            // bring O^T (PVs of the previous two pages done: they come from the two PV
+            // warps) to the new maxima (up or down)
+            bool got = tc::mbar_wait(bar(BAR_PV_DONE + (int)((j - 1) % kRing)),
+                                     (uint32_t)((j - 1) / kRing) & 1, kWaitNs);
+            if (got && j >= 2)
+              got = tc::mbar_wait(bar(BAR_PV_DONE + (int)((j - 2) % kRing)),
+                                  (uint32_t)((j - 2) / kRing) & 1, kWaitNs);
+            if (named_bar_softmax_or(!got)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
 #pragma unroll 1
-          for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-              uint32_t r[32];
-              const uint32_t ta = tmem + lane_base + kOCol + 64 * blk + 32 * half;
-              tc::tmem_ld32(ta, r);
+            for (int blk = 0; blk < 4; ++blk) {
+              uint32_t rr[32];
+              const uint32_t ta = tmem + lane_hi + kOCol + 64 * blk + 32 * g;
+              tc::tmem_ld32(ta, rr);
               tc::tmem_wait_ld();
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha_w[32 * half + i]);
-              tc::tmem_st32(ta, r);
+                rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha_s[32 * g + i]);
+              tc::tmem_st32(ta, rr);
             }
+            tc::tmem_wait_st();
           }
-          tc::tmem_wait_st();
         }
-        // ---- P = 2^(s - m + 6) as e4m3 hi + e5m2 lo, row h of P^T ----
+        // ---- P = 2^(s - m + 6) as e4m3 hi + e5m2 lo, this thread's 16 tokens of row h of P^T ----
         {
           const float mu = m == -INFINITY ? 0.f : m - (float)kPOffset;
-          uint32_t hw[8], lw[8];
+          uint32_t hw[4], lw[4];
           float rs = 0.f;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
+          for (int k = 0; k < 4; ++k) {
             uint32_t hcode[2], lcode[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -783,24 +837,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             hw[k] = hcode[0] | (hcode[1] << 16);
             lw[k] = lcode[0] | (lcode[1] << 16);
           }
-          rs += __shfl_xor_sync(0xffffffffu, rs, 16);
-          l += rs;
+          lpart += rs;
           const uint32_t prow = sbase + kOffP + (int)(j % kPBufs) * kPBytes + h * 128;
           const int sw = h & 7;
-#pragma unroll
-          for (int q2 = 0; q2 < 2; ++q2) {
-            const uint32_t ah = prow + (((2 * part + q2) ^ sw) << 4);
-            const uint32_t al = prow + (((4 + 2 * part + q2) ^ sw) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(ah), "r"(hw[4 * q2]),
-                         "r"(hw[4 * q2 + 1]), "r"(hw[4 * q2 + 2]), "r"(hw[4 * q2 + 3]));
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(al), "r"(lw[4 * q2]),
-                         "r"(lw[4 * q2 + 1]), "r"(lw[4 * q2 + 2]), "r"(lw[4 * q2 + 3]));
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + ((c16 ^ sw) << 4)),
+                       "r"(hw[0]), "r"(hw[1]), "r"(hw[2]), "r"(hw[3]));
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(prow + (((4 + c16) ^ sw) << 4)),
+                       "r"(lw[0]), "r"(lw[1]), "r"(lw[2]), "r"(lw[3]));
+        }
+        if (nvis < kPageSize) {
+          // value rows past the page's last token (all rows of a bad page id) become
+          // zeros before PV reads them: their weights are 0, and 0 times a stale
+          // NaN code would poison O (QK(j) has already read the page)
+          const uint32_t page_base = sbase + kOffPages + (int)(j % kRing) * kPageBytes;
+          for (int i = t; i < (kPageSize - nvis) * 32; i += kSmThreads) {
+            const int rrow = nvis + (i >> 5), u = i & 31;
+            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};\n" ::"r"(
+                             page_base + (u >> 3) * kLatBlock + rrow * 128 + (u & 7) * 16),
+                         "r"(0u));
           }
         }
         tc::fence_proxy_async_smem();
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(bar(BAR_P_FULL + (int)(j % kPBufs)));
+        if (t == 0) MLA_STAMP(kStSmP, j);
         if (pe) {
           // ---- epilogue: O^T / l -> this piece's partial slot ----
           {
@@ -811,43 +872,57 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tc::fence_after_sync();
+          if (t == 0) MLA_STAMP(kStEpiStart, piece);
           const int slot = d.slot;
-          if (part == 0) {
-            linv_s[h] = l > 0.f ? p.kv_scale / l : 0.f;
-            if (h < H)
-              p.ws.part_lse[(int64_t)slot * H + h] =
-                  l > 0.f ? (m - (float)kPOffset + log2f(l)) * kLn2 : -INFINITY;
-          }
+          const float lh = lpart + __shfl_xor_sync(0xffffffffu, lpart, 16);
+          if (lane < 16) lsum_s[g * 64 + h] = lh;
           int bad = 0;
           if (t == 0) {
             bad = flags[F_PIECE_BAD];
             flags[F_PIECE_BAD] = 0;
           }
           named_bar_softmax();
+          if (g == 0 && lane < 16) {
+            const float l = lsum_s[h] + lsum_s[64 + h];
+            linv_s[h] = l > 0.f ? p.kv_scale / l : 0.f;
+            if (h < H)
+              p.ws.part_lse[(int64_t)slot * H + h] =
+                  l > 0.f ? (m - (float)kPOffset + log2f(l)) * kLn2 : -INFINITY;
+          }
           if (t == 0) p.ws.piece_err[slot] = bad;
-          float* out = p.ws.part_out + (int64_t)slot * H * kDLatent + t;
-          const int nhalf = (H + 31) >> 5;
+          named_bar_softmax();
+          // O^T lane = dim 128*blk + 32*(w%4) + lane; this warp writes heads 32g .. 32g+31
+          if (32 * g < H) {
+            float* out = p.ws.part_out + (int64_t)slot * H * kDLatent + 32 * q4 + lane;
 #pragma unroll 1
-          for (int blk = 0; blk < 4; ++blk) {
-#pragma unroll 1
-            for (int half = 0; half < nhalf; ++half) {
-              uint32_t r[32];
-              tc::tmem_ld32(tmem + lane_base + kOCol + 64 * blk + 32 * half, r);
+            for (int blk = 0; blk < 4; ++blk) {
+              uint32_t rr[32];
+              tc::tmem_ld32(tmem + lane_hi + kOCol + 64 * blk + 32 * g, rr);
               tc::tmem_wait_ld();
-              float* o = out + (int64_t)(32 * half) * kDLatent + 128 * blk;
+              float* o = out + (int64_t)(32 * g) * kDLatent + 128 * blk;
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
-                if (32 * half + i < H)
-                  o[(int64_t)i * kDLatent] =
-                      (__uint_as_float(r[i]) * linv_s[32 * half + i]);
+                if (32 * g + i < H)
+                  o[(int64_t)i * kDLatent] = __uint_as_float(rr[i]) * linv_s[32 * g + i];
               }
             }
+          }
+          {
+            // O^T back to zero for the next piece
+            uint32_t zz[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) zz[i] = 0u;
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk)
+              tc::tmem_st32(tmem + lane_hi + kOCol + 64 * blk + 32 * g, zz);
+            tc::tmem_wait_st();
           }
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(bar(BAR_O_EMPTY));
+          if (t == 0) MLA_STAMP(kStEpiEnd, piece);
           m = -INFINITY;
-          l = 0.f;
+          lpart = 0.f;
           ++piece;
         }
       }
@@ -857,7 +932,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == kQkWarp) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kQkWarp0) tc::tmem_dealloc(tmem, kTmemCols);
+  if (tid == 0) MLA_STAMP(kStExit, 0);
 }
 
 // ---- query split: once per (request, draft) row, before the decode kernel ----

@@ -63,8 +63,11 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parit
   return true;
 }
 // Waits for the phase with the given parity to complete; false after `limit_ns`.
+// A non-blocking test comes first: a suspending test of a phase that has already
+// completed costs a few hundred cycles (measured), which on the MMA issuers'
+// path leaves the tensor pipe idle.
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(addr, parity)) return true;
+  if (mbar_test(addr, parity)) return true;
   return mbar_wait_slow(addr, parity, limit_ns);
 }
 
@@ -154,24 +157,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
-// 16 lanes x 32 columns, split between the half-warps: thread i < 16 reads lane
-// (lane base + i), columns [c, c + 32); thread 16 + i reads the same lane, columns
-// [c + 32, c + 64), where `taddr` carries the lane base (a multiple of 16 inside
-// the warp's quarter) and column c.
 // Brings a kernel-parameter tensor map into the descriptor cache ahead of its first use.
 __device__ __forceinline__ void prefetch_tensormap(const void* map) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map))
                : "memory");
 }
-__device__ __forceinline__ void tmem_ld16x2_32(uint32_t taddr, uint32_t (&r)[32]) {
+// 16 lanes x 16 columns, split between the half-warps: thread i < 16 reads lane
+// (lane base + i), columns [c, c + 16); thread 16 + i reads the same lane, columns
+// [c + 16, c + 32), where `taddr` carries the lane base (a multiple of 16 inside
+// the warp's quarter) and column c.
+__device__ __forceinline__ void tmem_ld16x2_16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], 32;\n"
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16], 16;\n"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
