@@ -11,6 +11,7 @@
 
 #include "mla_common.cuh"
 #include "mla_internal.h"
+#include "merge_pieces.cuh"
 #include "tc_ptx.cuh"
 
 namespace mla {
@@ -77,24 +78,9 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ out_base, in
   if (tid == 0) *lse_out = empty ? -INFINITY : m + logf(total);
 }
 
-// Merge of mla_decode's pieces. One block per (row, head, quarter of the 512 dims).
-// The pieces' 128-dim slices (512 B each) are brought into shared memory by bulk
-// copies, up to kStagePieces at a time: a per-thread load stream keeps far fewer
-// bytes in flight per SM than the copy engine, and at batch 1 every block reads
-// about 150 slices. While they land, the threads read the pieces' lse and error
-// flags and form the weights exp(lse_s - max); then warp w sums pieces w, w + 8,
-// ... from shared memory (lane = 4 dims) and the warps' sums are added.
-constexpr int kPieceThreads = 256;
-constexpr int kPieceWarps = kPieceThreads / 32;
-constexpr int kQuarters = 4;
-// Slices staged per round: at most 160 (80 KB: one round for a row split over 152
-// CTAs); the launch picks about twice the average pieces per row, so that many
-// blocks fit on an SM when rows are many and short.
-constexpr int kStagePieces = 160;
-constexpr int kSliceBytes = 128 * 4;
-constexpr uint64_t kCombineWaitNs = 2000000000ull;
-
-__global__ void __launch_bounds__(kPieceThreads)
+// Merge of mla_decode's pieces: one block of kMergeThreads per unit (row, head,
+// quarter of the 512 dims), see merge_unit.
+__global__ void __launch_bounds__(kMergeThreads)
 combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __restrict__ row_np,
                       const int32_t* __restrict__ piece_err, const float* __restrict__ part_lse,
                       const float* __restrict__ part_out, int heads,
@@ -105,111 +91,18 @@ combine_pieces_kernel(const int32_t* __restrict__ row_base, const int32_t* __res
   griddep_launch_dependents();
   extern __shared__ float4 stage[];                 // [stage_pieces][32] float4
   __shared__ __align__(8) uint64_t mbar;
-  __shared__ float s_w[kStagePieces];
-  __shared__ float4 s_acc[kPieceWarps][32];
-  __shared__ float s_red[kPieceWarps];
-  const int64_t blk = blockIdx.x;
-  const int quarter = (int)(blk % kQuarters);
-  const int64_t rh = blk / kQuarters;
-  const int r = (int)(rh / heads);
-  const int h = (int)(rh - (int64_t)r * heads);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int np = __ldcg(row_np + r);
-  const int base = __ldcg(row_base + r);
+  __shared__ MergeShared sm;
   const uint32_t mb = smem_u32(&mbar);
-  // The first round's copies go out before anything else is read: their slices
-  // do not depend on the weights, so they land while the lse values are read.
-  const int n0 = min(stage_pieces, max(np, 0));
-  if (tid == 0) {
+  if (threadIdx.x == 0) {
     tc::mbar_init(mb, 1);
     tc::fence_mbar_init();
-    if (n0 > 0) tc::mbar_arrive_expect_tx(mb, (uint32_t)(n0 * kSliceBytes));
   }
-  __syncthreads();
-  if (tid < n0)
-    tc::bulk_load(smem_u32(stage + 32 * tid),
-                  part_out + ((int64_t)(base + tid) * heads + h) * kDLatent + 128 * quarter,
-                  kSliceBytes, mb);
-  // the block's maximum lse and whether any piece met a bad page
-  float m = -INFINITY, l_own = -INFINITY;
-  int bad = 0;
-  for (int s = tid; s < np; s += kPieceThreads) {
-    const float l = __ldcg(part_lse + (int64_t)(base + s) * heads + h);
-    if (s == tid) l_own = l;
-    m = fmaxf(m, l);
-    bad |= __ldcg(piece_err + base + s);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) s_red[warp] = m;
-  bad = __syncthreads_or(bad);
-  m = s_red[0];
-#pragma unroll
-  for (int w = 1; w < kPieceWarps; ++w) m = fmaxf(m, s_red[w]);
-  const bool empty = np <= 0 || bad || !(m > -INFINITY);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;   // this thread's share of the weights (threads of lane 0 only)
-  bool timed_out = false;
   uint32_t phase = 0;
-  for (int c0 = 0; c0 < np; c0 += stage_pieces) {
-    const int n = min(stage_pieces, np - c0);
-    if (c0 > 0) {  // later rounds (more pieces than the stage holds)
-      __syncthreads();  // the previous round's slices and weights are no longer read
-      if (tid == 0) tc::mbar_arrive_expect_tx(mb, (uint32_t)(n * kSliceBytes));
-      __syncthreads();
-      if (tid < n) {
-        const int64_t piece = (int64_t)(base + c0 + tid) * heads + h;
-        tc::bulk_load(smem_u32(stage + 32 * tid), part_out + piece * kDLatent + 128 * quarter,
-                      kSliceBytes, mb);
-      }
-    }
-    if (tid < n) {
-      const float l = c0 == 0 ? l_own : __ldcg(part_lse + (int64_t)(base + c0 + tid) * heads + h);
-      s_w[tid] = (l > -INFINITY && !empty) ? fast_exp2((l - m) * kLog2e) : 0.f;
-    }
-    __syncthreads();
-    // every issued copy is waited for, also for a row whose result is empty
-    if (!tc::mbar_wait(mb, phase, kCombineWaitNs)) {
-      // never expected: record it and give the copies one more bound to land
-      // before their shared memory is read or the block exits
-      timed_out = true;
-      tc::mbar_wait(mb, phase, kCombineWaitNs);
-    }
-    phase ^= 1u;
-    if (!empty) {
-      for (int s = warp; s < n; s += kPieceWarps) {
-        const float w = s_w[s];
-        if (w == 0.f) continue;  // empty piece: its slice is never used
-        const float4 v = stage[32 * s + lane];
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-        if (lane == 0) wsum += w;
-      }
-    }
-  }
-  if (__syncthreads_or(timed_out ? 1 : 0)) {
-    if (tid == 0) atomicOr(status, MLA_DEVICE_ERR_TIMEOUT);
-  }
-  s_acc[warp][lane] = acc;
-  if (lane == 0) s_red[warp] = wsum;
-  __syncthreads();
-  if (warp == 0) {
-    float total = 0.f;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int w = 0; w < kPieceWarps; ++w) {
-      total += s_red[w];
-      const float4 b = s_acc[w][lane];
-      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
-    }
-    const float inv = empty ? 0.f : 1.0f / total;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * inv, a.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * inv, a.w * inv);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(out + rh * kDLatent + 128 * quarter + 4 * lane) = packed;
-    if (quarter == 0 && lane == 0) lse[rh] = empty ? -INFINITY : m + logf(total);
-  }
+  const bool ok = merge_unit(
+      blockIdx.x, heads, row_base, row_np, piece_err, part_lse, part_out, out, lse, stage_pieces,
+      stage, sm, mb, phase, (int)threadIdx.x, [] { __syncthreads(); },
+      [](bool pred) { return __syncthreads_or(pred ? 1 : 0) != 0; });
+  if (!ok && threadIdx.x == 0) atomicOr(status, MLA_DEVICE_ERR_TIMEOUT);
 }
 
 // Standalone merge: part_out [S][rows][512], part_lse [S][rows]; one block per row.
@@ -228,7 +121,7 @@ combine_dense_kernel(const float* __restrict__ part_out, const float* __restrict
 cudaError_t launch_combine_pieces(const DecodeWorkspace& ws, int rows, int heads,
                                   int max_pieces_per_row, __nv_bfloat16* out, float* lse,
                                   cudaStream_t stream) {
-  const unsigned blocks = (unsigned)((int64_t)rows * heads * kQuarters);
+  const unsigned blocks = (unsigned)((int64_t)rows * heads * kMergeQuarters);
 
   static std::atomic<int> configured[64];
   int dev = 0;
@@ -236,16 +129,15 @@ cudaError_t launch_combine_pieces(const DecodeWorkspace& ws, int rows, int heads
   if (dev >= 0 && dev < 64 && !configured[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(combine_pieces_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kStagePieces * kSliceBytes);
+                                         kMergeStagePieces * (int)kMergeSliceBytes);
     if (e != cudaSuccess) return e;
     configured[dev].store(1);
   }
-  const int64_t per_row = 2 * (int64_t)max_pieces_per_row / max(rows, 1) + 2;
-  const int stage = (int)std::min<int64_t>(kStagePieces, std::max<int64_t>(16, per_row));
+  const int stage = merge_stage_pieces(max_pieces_per_row, rows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks);
-  cfg.blockDim = dim3(kPieceThreads);
-  cfg.dynamicSmemBytes = (size_t)stage * kSliceBytes;
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = (size_t)stage * kMergeSliceBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1] = {pdl_attribute()};
   cfg.attrs = attr;

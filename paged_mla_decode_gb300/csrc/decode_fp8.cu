@@ -907,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          {
+          if (j + 1 < npages) {
             // O^T back to zero for the next piece
             uint32_t zz[32];
 #pragma unroll
@@ -1087,6 +1087,7 @@ cudaError_t launch_decode_fp8(const DecodeLaunch& d, cudaStream_t stream) {
   if (dev >= 0 && dev < 64 && !configured[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(decode_fp8_kernel<true>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytesGrouped);
