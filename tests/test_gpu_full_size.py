@@ -21,9 +21,10 @@ from .gpu_util import assert_close, gpu_decode, gpu_fill_cache
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 
-def _check_sampled(w, pages, dev, samples, kv_dtype="e4m3"):
+def _check_sampled(w, pages, dev, samples, kv_dtype="e4m3", f16_operands=False):
     kv_scale = w.kv_scale if kv_dtype == "e4m3" else 1.0
-    out, lse, ws = gpu_decode(w, pages, dev, kv_scale=kv_scale)
+    out, lse, ws = gpu_decode(w, pages, dev, kv_scale=kv_scale, f16_operands=f16_operands)
+    path = "f16 operands" if f16_operands else kv_dtype
     flat = pages.view(-1, 576)
     for b in samples:
         bits = w.request_latent(b)
@@ -47,7 +48,7 @@ def _check_sampled(w, pages, dev, samples, kv_dtype="e4m3"):
             # the relative term on its own (the absolute one carries the combined
             # tolerance where a nearly flat softmax makes |out| ~ 1e-3)
             rel = float(np.abs(out[b, j] - ref_out).max() / np.abs(ref_out).max())
-            print(f"{w.name} {kv_dtype} b={b} j={j}: max|ref| {np.abs(ref_out).max():.3g} "
+            print(f"{w.name} {path} b={b} j={j}: max|ref| {np.abs(ref_out).max():.3g} "
                   f"rel err {rel:.3g} lse err {lerr:.3g}")
             assert rel <= 1e-2, f"{w.name} b={b} j={j}: relative error {rel:.4g}"
     return out, lse, ws
@@ -72,14 +73,29 @@ def test_prefix_shared(cuda_device):
     _check_sampled(w, pages, cuda_device, [0, 1, 2, 3, 45])
 
 
-def test_speculative(cuda_device):
-    w = wl.speculative()
-    pages = gpu_fill_cache(w, cuda_device)
+def _speculative_cache(w, dev):
+    pages = gpu_fill_cache(w, dev)
     # the step's new tokens go in through the same append path
     fresh = torch.from_numpy(w.fresh_token_latent().view(np.int16)).view(torch.bfloat16)
-    fresh = fresh.to(cuda_device)
+    fresh = fresh.to(dev)
     from paged_mla_decode_gb300 import binding
     binding.mla_kv_append(fresh[:, :512].contiguous(), fresh[:, 512:].contiguous(),
-                          torch.from_numpy(w.fresh_token_slots()).to(cuda_device), pages,
-                          w.kv_scale)
-    _check_sampled(w, pages, cuda_device, [0, 13, 31])
+                          torch.from_numpy(w.fresh_token_slots()).to(dev), pages, w.kv_scale)
+    return pages
+
+
+def test_speculative(cuda_device):
+    w = wl.speculative()
+    _check_sampled(w, _speculative_cache(w, cuda_device), cuda_device, [0, 13, 31])
+
+
+@pytest.mark.parametrize("name", ["long", "speculative"])
+def test_f16_operands_full_size(cuda_device, name):
+    # the ablation (e4m3 pages widened to f16 operands) at full length, 152-way split
+    if name == "long":
+        w = wl.long_context()
+        pages, samples = gpu_fill_cache(w, cuda_device), [0]
+    else:
+        w = wl.speculative()
+        pages, samples = _speculative_cache(w, cuda_device), [0, 31]
+    _check_sampled(w, pages, cuda_device, samples, f16_operands=True)
