@@ -608,8 +608,9 @@ def run_gpu(args):
             "logical_kv_gbs": world * accounting.step_bytes(w.seq_lens, Q, H, kv_dtype)["kv"]
             * steps_per_s / 1e9,
             "cpu_baseline": cpu, "e2e": e2e, "kv_check": kv_check,
-            # per step: KV append, then mla_decode's query split, decode and combine
-            "gpu_launches": 4 * args.steps, "clocks": clocks,
+            # per step: KV append, then the decode call's kernels (query split, decode,
+            # combine; the grouped decode also plans its row table first)
+            "gpu_launches": (5 if grouped else 4) * args.steps, "clocks": clocks,
             "decode_call_us": {"mean": decode_us, "median": decode_us_median,
                                "samples": len(decode_ms)},
             "device_status": status,

@@ -493,7 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  bar(BAR_PAGE_FULL + slot), pol);
             MLA_STAMP(kStTmaIssue, j);
           } else {
-            tc::mbar_arrive(bar(BAR_PAGE_FULL + slot));  // bad id: the MMA warp zero-fills
+            // bad id: no copy; every token of the page is masked and the softmax
+            // warps zero its value rows before PV reads them
+            tc::mbar_arrive(bar(BAR_PAGE_FULL + slot));
           }
           for (int u = 0; u < 2 && jn < npages && jn <= j + kTableAhead; ++u) describe_next();
         }
