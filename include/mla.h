@@ -70,7 +70,7 @@ typedef struct CUstream_st* mla_stream_t;
 typedef enum mla_status {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1, /* a null pointer, a bad size, a misaligned buffer */
-  MLA_ERR_UNSUPPORTED = 2, /* a shape this build has no kernel for */
+  MLA_ERR_UNSUPPORTED = 2, /* a shape the library has no kernel for */
   MLA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
   MLA_ERR_CUDA = 4         /* a CUDA runtime call or a launch failed */
 } mla_status;
